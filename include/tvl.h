@@ -1,0 +1,189 @@
+/*
+ * tvl.h -- C ABI of libtvl.so, a GB300 (sm_103a) implementation of the paged
+ * attention hot path: the slot-mapped paged KV-cache write, PagedAttention
+ * decode (single pass or split-K with a log-sum-exp merge) and chunked causal
+ * prefill over a cached prefix.
+ *
+ * Sources of the method (web pages on tiny-vLLM and nano-vLLM):
+ *   [tiny-vllm README]  "tiny-vllm" README, Korean translation: feature list
+ *                       ("KV cache", "online softmax, FlashAttention style",
+ *                       "PagedAttention") and the curriculum entries
+ *                       "Attention", "GQA", "Softmax", "Causal mask",
+ *                       "Prefill vs decode", "Online softmax",
+ *                       "Paged Attention", "Paged KV cache",
+ *                       "Paged Attention CUDA kernel".
+ *   [Tiny-vLLM digest]  "Tiny-vLLM: C++와 CUDA로 만드는 고성능 LLM 추론 엔진",
+ *                       section "Core Mechanics" (bf16, every op a CUDA
+ *                       kernel, KV cache, online softmax, PagedAttention, GQA,
+ *                       causal mask) and section "Evidence" (CUDA return codes
+ *                       must be checked).
+ *   [nano-vLLM guide]   "LLM 추론(Inference)이 실제로 어떻게 작동하는지에 대한 11장
+ *                       분량의 인터랙티브 가이드", chapter 4 "PagedAttention" (the
+ *                       KV cache as virtual memory made of fixed-size blocks),
+ *                       chapter 6 "Prefill vs Decode", chapter 7 "Prefix
+ *                       Caching", chapter 10 "The Optimization Stack".
+ *
+ * Common conventions
+ * ------------------
+ * Shapes: S = num_seqs, Hq = num_q_heads, Hkv = num_kv_heads, G = Hq / Hkv,
+ *   D = head_dim, bs = block_size, NB = num_blocks (physical blocks in the
+ *   pool), MB = max_blocks_per_seq (columns of block_tables).
+ * Element types: q, K and V are bfloat16 (passed as void*, 2 bytes each);
+ *   attention outputs are float32; all metadata is int32.
+ * Cache layout: k_cache and v_cache are each a contiguous bf16 array
+ *   [NB, bs, Hkv, D].  Token slot `x = block * bs + offset` is row x of the
+ *   flat view [NB * bs, Hkv * D]; one physical block is one contiguous run of
+ *   bs * Hkv * D * 2 bytes.
+ * Block table: block_tables is int32 [S, MB], row-major.  Logical token j of
+ *   sequence s lives in physical block block_tables[s * MB + j / bs], at
+ *   offset j % bs.  Entries at or beyond ceil(context_lens[s] / bs) are never
+ *   read.  Two rows may name the same physical block (shared prefixes).
+ * GQA: query head h reads KV head h / G.
+ * Scores: s_j = scale * sum_d q[d] * k_j[d], accumulated in float32.
+ * Pointers: every pointer except `stream` and a zero-size workspace is a
+ *   device pointer, owned by the caller, and must be 16-byte aligned.  The
+ *   library allocates no device memory and frees nothing.
+ * Streams: every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *   legacy default stream).  A non-OK return means nothing was launched.
+ * Errors: arguments are validated on the host before any launch.  Kernels
+ *   never trap: an out-of-range block id, slot or context length found on the
+ *   device is replaced by a safe value, the work it touches is undefined, and
+ *   a bit is set in a per-device status word read by tvl_get_device_status().
+ * Threads: calls are thread-safe; tvl_last_error() is per thread.
+ */
+#ifndef TVL_H
+#define TVL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TVL_OK = 0,
+  TVL_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or shape     */
+  TVL_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. head_dim 128)  */
+  TVL_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required     */
+  TVL_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed              */
+  TVL_ERR_DEVICE_CHECK = 5   /* a kernel found bad metadata (status word set)  */
+} tvl_status;
+
+/* Bits of the device status word (tvl_get_device_status). */
+#define TVL_DEV_BAD_SLOT        0x1  /* slot_mapping entry >= NB * bs            */
+#define TVL_DEV_BAD_BLOCK_ID    0x2  /* block table entry outside [0, NB)        */
+#define TVL_DEV_BAD_CONTEXT_LEN 0x4  /* context length < 0 or > MB * bs          */
+#define TVL_DEV_BAD_QUERY_LEN   0x8  /* prefill: query length > context length   */
+
+/*
+ * Paged KV write [tiny-vllm README, curriculum "Paged KV cache" and "Why KV
+ * cache exists"]: for every t in [0, T) with slot_mapping[t] >= 0,
+ *   k_cache row slot_mapping[t] <- k_new[t]   and   v_cache row <- v_new[t],
+ * where a row is Hkv * D bf16 values.  Rows with a negative slot are skipped.
+ * The copy is bit-exact.  Slots must be distinct (duplicates: which writer
+ * wins is unspecified).  A slot >= NB * bs is skipped and sets
+ * TVL_DEV_BAD_SLOT.
+ *   k_new, v_new : bf16 [T, Hkv, D]   (device, read)
+ *   k_cache, v_cache : bf16 [NB, bs, Hkv, D] (device, written in place)
+ *   slot_mapping : int32 [T]          (device, read)
+ * T == 0 is valid and launches nothing.  Supported: D in {64};
+ * Hkv * D * 2 a multiple of 16 bytes.
+ */
+tvl_status tvl_paged_kv_write(const void* k_new, const void* v_new,
+                              void* k_cache, void* v_cache,
+                              const int32_t* slot_mapping, int num_tokens,
+                              int num_kv_heads, int head_dim, int block_size,
+                              int num_blocks, void* stream);
+
+/*
+ * Workspace needed by tvl_paged_attention_decode for these sizes, written to
+ * *bytes.  partition_size has the same meaning as in the decode call.  With
+ * partition_size == 0 the answer depends on the current device's SM count.
+ * A zero answer means the call needs no workspace.
+ */
+tvl_status tvl_paged_attention_decode_workspace_size(
+    int num_seqs, int num_q_heads, int head_dim, int max_blocks_per_seq,
+    int block_size, int partition_size, size_t* bytes);
+
+/*
+ * PagedAttention decode [tiny-vllm README, curriculum "Attention", "GQA",
+ * "Softmax", "Online softmax", "Paged Attention", "Paged Attention CUDA
+ * kernel"; nano-vLLM guide ch. 4 "PagedAttention", ch. 6 "Prefill vs Decode"]:
+ * one query token per sequence attends to all context_lens[s] cached tokens
+ * of that sequence (the token written by this step's tvl_paged_kv_write is
+ * included; no mask):
+ *   out[s, h, :] = sum_j softmax_j(s_j) * V_j,   j in [0, context_lens[s]),
+ * with K_j, V_j gathered through the block table from KV head h / G.
+ * context_lens[s] == 0 gives a zero output row.
+ *   out          : float32 [S, Hq, D]  (device, written)
+ *   q            : bf16 [S, Hq, D]     (device, read)
+ *   block_tables : int32 [S, MB]; context_lens : int32 [S] (device, read)
+ * partition_size selects how the context is split (all splits are merged
+ * exactly by log-sum-exp, the associative form of the online softmax):
+ *   0   the library balances the total block count evenly over one CTA per
+ *       SM; a sequence may be cut anywhere on a block boundary.
+ *   >0  fixed windows [p * P, (p + 1) * P) of P tokens from position 0 (the
+ *       last one partial); P must be a multiple of block_size.  P >= MB * bs
+ *       is a single pass per sequence and needs no workspace.
+ * workspace: device memory of at least the size reported by
+ *   tvl_paged_attention_decode_workspace_size (may be NULL when that is 0);
+ *   its contents on entry are ignored and on exit unspecified.
+ * Supported: D == 64, G in {1, 2, 4, 8}, bs in {16, 32}, Hkv <= 8 or a
+ * multiple of 8.
+ */
+tvl_status tvl_paged_attention_decode(
+    float* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+    int num_blocks, int max_blocks_per_seq, float scale, int partition_size,
+    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Chunked causal prefill over a cached prefix [tiny-vllm README, curriculum
+ * "Prefill vs decode", "Attention", "GQA", "Causal mask", "Online softmax",
+ * "Paged Attention"; nano-vLLM guide ch. 6 "Prefill vs Decode", ch. 7
+ * "Prefix Caching", ch. 10 "The Optimization Stack" (FlashAttention)]:
+ * sequence s owns query tokens [query_start_loc[s], query_start_loc[s+1]),
+ * Lq = their count, which are the LAST Lq tokens of its context_lens[s]
+ * tokens; their K/V must already be in the paged cache (tvl_paged_kv_write).
+ * Query row i sits at absolute position p = context_lens[s] - Lq + i and
+ * attends to cached tokens 0..p inclusive (causal):
+ *   out[t, h, :] = sum_{j<=p} softmax_j(s_j) * V_j.
+ *   out  : float32 [Tq, Hq, D]; q : bf16 [Tq, Hq, D]        (device)
+ *   query_start_loc : int32 [S + 1], non-decreasing, [0] = 0, [S] = Tq
+ *   block_tables : int32 [S, MB]; context_lens : int32 [S]  (device)
+ * max_q_len must be >= every Lq (it sizes the grid).  Lq > context_lens[s]
+ * is invalid on the device (rows are left unwritten, TVL_DEV_BAD_QUERY_LEN).
+ * Supported: D == 64, G in {1, 2, 4, 8}, bs in {16, 32, 64, 128}, Hkv <= 255.
+ */
+tvl_status tvl_paged_attention_prefill(
+    float* out, const void* q, const int32_t* query_start_loc,
+    const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, int num_seqs, int total_q_tokens,
+    int max_q_len, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, int num_blocks, int max_blocks_per_seq, float scale,
+    void* stream);
+
+/* Static description of a status code. */
+const char* tvl_status_string(tvl_status status);
+
+/* Detail of the last non-OK return on the calling thread ("" if none). */
+const char* tvl_last_error(void);
+
+/*
+ * Reads and clears the current device's status word (TVL_DEV_* bits).  The
+ * read is ordered after all prior work on `stream` and synchronises it.
+ * Returns TVL_OK when the word was zero, TVL_ERR_DEVICE_CHECK when a bit was
+ * set (the bits go to *bits if bits != NULL), TVL_ERR_CUDA on a CUDA error.
+ */
+tvl_status tvl_get_device_status(void* stream, uint32_t* bits);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int tvl_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TVL_H */
