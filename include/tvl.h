@@ -98,13 +98,15 @@ tvl_status tvl_paged_kv_write(const void* k_new, const void* v_new,
 
 /*
  * Workspace needed by tvl_paged_attention_decode for these sizes, written to
- * *bytes.  partition_size has the same meaning as in the decode call.  With
- * partition_size == 0 the answer depends on the current device's SM count.
- * A zero answer means the call needs no workspace.
+ * *bytes.  The arguments mean what they mean in the decode call and are
+ * validated the same way.  With partition_size == 0 the answer depends on the
+ * current device's SM count.  A zero answer means the call needs no
+ * workspace.
  */
 tvl_status tvl_paged_attention_decode_workspace_size(
-    int num_seqs, int num_q_heads, int head_dim, int max_blocks_per_seq,
-    int block_size, int partition_size, size_t* bytes);
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int max_blocks_per_seq, int block_size, int partition_size,
+    size_t* bytes);
 
 /*
  * PagedAttention decode [tiny-vllm README, curriculum "Attention", "GQA",

@@ -1,0 +1,217 @@
+"""Paged attention for GB300: Python binding of libtvl.so.
+
+Thin argument marshalling over the C ABI declared in ``include/tvl.h``:
+torch CUDA tensors are checked (dtype, device, shape, contiguity) and passed as
+raw pointers with the current CUDA stream.  Every step of the computation runs
+in the library's CUDA kernels; there is no fallback.  If ``libtvl.so`` has not
+been built, every call raises ``TvlError``.
+
+Functions (same names as the C entry points, without the ``tvl_`` prefix):
+  paged_kv_write, paged_attention_decode, paged_attention_decode_workspace_size,
+  paged_attention_prefill, get_device_status, version.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "TvlError", "paged_kv_write", "paged_attention_decode",
+    "paged_attention_decode_workspace_size", "paged_attention_prefill", "get_device_status",
+    "version", "library_path", "DEV_BAD_SLOT", "DEV_BAD_BLOCK_ID", "DEV_BAD_CONTEXT_LEN",
+    "DEV_BAD_QUERY_LEN", "DEV_TIMEOUT",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libtvl.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_CHECK = range(6)
+DEV_BAD_SLOT, DEV_BAD_BLOCK_ID, DEV_BAD_CONTEXT_LEN, DEV_BAD_QUERY_LEN, DEV_TIMEOUT = (
+    0x1, 0x2, 0x4, 0x8, 0x10)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class TvlError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__(f"tvl status {status}: {detail}")
+        self.status = status
+        self.detail = detail
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise TvlError(ERR_CUDA, f"{_LIB_PATH} is missing: build it with "
+                                         "paged_kv_cache_198_gb300._build.build()")
+            lib = ctypes.CDLL(_LIB_PATH)
+            P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            lib.tvl_paged_kv_write.argtypes = [P, P, P, P, P, I, I, I, I, I, P]
+            lib.tvl_paged_attention_decode_workspace_size.argtypes = [
+                I, I, I, I, I, I, I, ctypes.POINTER(SZ)]
+            lib.tvl_paged_attention_decode.argtypes = [
+                P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, SZ, P]
+            lib.tvl_paged_attention_prefill.argtypes = [
+                P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P]
+            lib.tvl_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+            for name in ("tvl_paged_kv_write", "tvl_paged_attention_decode_workspace_size",
+                         "tvl_paged_attention_decode", "tvl_paged_attention_prefill",
+                         "tvl_get_device_status"):
+                getattr(lib, name).restype = I
+            lib.tvl_status_string.argtypes = [I]
+            lib.tvl_status_string.restype = ctypes.c_char_p
+            lib.tvl_last_error.argtypes = []
+            lib.tvl_last_error.restype = ctypes.c_char_p
+            lib.tvl_version.argtypes = []
+            lib.tvl_version.restype = I
+            _lib = lib
+    return _lib
+
+
+def _check(rc: int) -> None:
+    if rc != OK:
+        lib = _load()
+        raise TvlError(rc, (lib.tvl_last_error() or b"").decode() or
+                       lib.tvl_status_string(rc).decode())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+
+
+def version() -> int:
+    return int(_load().tvl_version())
+
+
+def paged_kv_write(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None) -> None:
+    """k_cache/v_cache bf16 [NB, bs, Hkv, D] (in place) <- k_new/v_new bf16
+    [T, Hkv, D] at rows slot_mapping int32 [T] (negative = skip)."""
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    dev = k_cache.device
+    _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _need(k_new, "k_new", torch.bfloat16, 3, dev)
+    _need(v_new, "v_new", torch.bfloat16, 3, dev)
+    _need(slot_mapping, "slot_mapping", torch.int32, 1, dev)
+    nb, bs, hkv, d = k_cache.shape
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    t = slot_mapping.shape[0]
+    if k_new.shape != (t, hkv, d) or v_new.shape != (t, hkv, d):
+        raise ValueError(f"k_new/v_new must be [{t}, {hkv}, {d}]")
+    with torch.cuda.device(dev):
+        _check(_load().tvl_paged_kv_write(_ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                          _ptr(v_cache), _ptr(slot_mapping), t, hkv, d, bs, nb,
+                                          _stream(stream)))
+
+
+def paged_attention_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                          max_blocks_per_seq, block_size,
+                                          partition_size=0) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_load().tvl_paged_attention_decode_workspace_size(
+        num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size,
+        partition_size, ctypes.byref(out)))
+    return int(out.value)
+
+
+def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                           partition_size=0, workspace=None, stream=None):
+    """out fp32 [S, Hq, D] <- paged decode attention of q bf16 [S, Hq, D].
+    workspace: uint8 CUDA tensor (allocated here when None and needed)."""
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    dev = k_cache.device
+    _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _need(q, "q", torch.bfloat16, 3, dev)
+    _need(out, "out", torch.float32, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    nb, bs, hkv, d = k_cache.shape
+    s, hq, d2 = q.shape
+    if d2 != d or out.shape != q.shape or v_cache.shape != k_cache.shape:
+        raise ValueError("inconsistent q / out / cache shapes")
+    if block_tables.shape[0] != s or context_lens.shape[0] != s:
+        raise ValueError("block_tables / context_lens must have num_seqs rows")
+    mb = block_tables.shape[1]
+    with torch.cuda.device(dev):
+        need = paged_attention_decode_workspace_size(s, hq, hkv, d, mb, bs, partition_size)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        if workspace is not None:
+            _need(workspace, "workspace", torch.uint8, 1, dev)
+        ws_bytes = workspace.numel() if workspace is not None else 0
+        _check(_load().tvl_paged_attention_decode(
+            _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+            _ptr(context_lens), s, hq, hkv, d, bs, nb, mb, float(scale), int(partition_size),
+            _ptr(workspace), ws_bytes, _stream(stream)))
+    return out
+
+
+def paged_attention_prefill(out, q, query_start_loc, k_cache, v_cache, block_tables,
+                            context_lens, scale, max_q_len, stream=None):
+    """out fp32 [Tq, Hq, D] <- causal attention of the last Lq tokens of each
+    sequence (q bf16 [Tq, Hq, D], packed by query_start_loc int32 [S+1])."""
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    dev = k_cache.device
+    _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _need(q, "q", torch.bfloat16, 3, dev)
+    _need(out, "out", torch.float32, 3, dev)
+    _need(query_start_loc, "query_start_loc", torch.int32, 1, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    nb, bs, hkv, d = k_cache.shape
+    tq, hq, d2 = q.shape
+    s = context_lens.shape[0]
+    if d2 != d or out.shape != q.shape or v_cache.shape != k_cache.shape:
+        raise ValueError("inconsistent q / out / cache shapes")
+    if query_start_loc.shape[0] != s + 1 or block_tables.shape[0] != s:
+        raise ValueError("query_start_loc must be [S+1] and block_tables [S, MB]")
+    mb = block_tables.shape[1]
+    with torch.cuda.device(dev):
+        _check(_load().tvl_paged_attention_prefill(
+            _ptr(out), _ptr(q), _ptr(query_start_loc), _ptr(k_cache), _ptr(v_cache),
+            _ptr(block_tables), _ptr(context_lens), s, tq, int(max_q_len), hq, hkv, d, bs, nb,
+            mb, float(scale), _stream(stream)))
+    return out
+
+
+def get_device_status(stream=None) -> int:
+    """Reads and clears the device status word; returns its bits (0 = clean).
+    Synchronises the stream."""
+    bits = ctypes.c_uint32(0)
+    rc = _load().tvl_get_device_status(_stream(stream), ctypes.byref(bits))
+    if rc not in (OK, ERR_DEVICE_CHECK):
+        _check(rc)
+    return int(bits.value)

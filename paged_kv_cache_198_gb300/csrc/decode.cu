@@ -1,0 +1,878 @@
+// decode.cu -- PagedAttention decode with online softmax, GQA and split-K.
+//
+// What it computes [tiny-vllm README, curriculum "Attention", "GQA",
+// "Softmax", "Online softmax", "Paged Attention", "Paged Attention CUDA
+// kernel"]: for each sequence s and query head h,
+//   out[s,h,:] = sum_j softmax_j(scale * q[s,h,:] . K_j) V_j,
+// K_j / V_j being token j of KV head h / G, found through the block table
+// [nano-vLLM guide ch. 4 "PagedAttention": fixed-size blocks, like pages of
+// virtual memory].  Decode is memory-bound [nano-vLLM guide ch. 6 "Prefill vs
+// Decode"], so the design streams each cached K/V byte from HBM exactly once.
+//
+// Work split.  The context of every sequence is cut on physical-block
+// boundaries into segments:
+//   * balanced mode (partition_size 0): the flattened list of all sequences'
+//     blocks is divided evenly over one CTA per SM (per KV-head group), so
+//     each CTA streams the same number of blocks whatever the length mix;
+//   * fixed mode (partition_size P): windows of P tokens from position 0,
+//     one CTA each.
+// A segment that covers its whole sequence writes the final output; any other
+// writes a partial (m, l, acc) record, and merge_kernel combines the records
+// of a sequence by log-sum-exp -- the associative form of the online softmax.
+//
+// CTA structure.  One producer warp walks the CTA's segments and, per
+// physical block, issues 1-D bulk copies (TMA engine) of the block's K and V
+// for the CTA's KV heads (bs * Hkv * D * 2 contiguous bytes each when the CTA
+// owns every KV head) into a ring of shared-memory stages, with an mbarrier
+// per stage.  One consumer warp per KV head computes, per 16-token chunk:
+//   * q . k with lane = 8 * token_group + dim_chunk: each lane holds 8 dims
+//     of the G query heads (fp32, pre-scaled by scale * log2 e) and reads
+//     8 dims of 4 tokens (16-byte shared loads, conflict-free), packed
+//     fp32x2 FMAs; the 8-lane partial sums of the 4G (head, token) pairs are
+//     reduced with a transposing butterfly (4G/8 values per lane remain;
+//     the register order is permuted per lane so no selects are needed);
+//   * an online softmax in the exp2 domain whose running maximum is only
+//     moved when a score exceeds it by more than 2^8 (exact: the same
+//     reference maximum scales numerator and denominator);
+//   * p . V with p staged through a per-warp shared buffer, fp32x2 FMAs.
+// All waits are bounded; a timeout sets a status bit and the CTA leaves
+// after its copies in flight have landed.
+#include <cuda_bf16.h>
+
+#include "device.cuh"
+#include "kernels.h"
+
+namespace tvl {
+namespace {
+
+constexpr int kD = 64;
+constexpr uint32_t kRowBytes = kD * 2;   // one head's K or V row of one token
+constexpr int kChunk = 16;
+constexpr int kMaxHeadsPerCta = 8;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr unsigned kFull = 0xffffffffu;
+constexpr uint32_t kSmemBudget = 224 * 1024;
+
+enum : int { kSegFirst = 1, kSegLast = 2, kTerminate = 4 };
+
+struct StageMeta {
+  int seq;
+  int valid;    // tokens of this block inside the context
+  int flags;
+  int record;   // -1: final output, else partial record index
+};
+
+struct Params {
+  float* out;
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k_cache;
+  const __nv_bfloat16* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int num_seqs, hq, hkv, num_blocks, max_blocks;
+  int hpc;               // KV heads per CTA == consumer warps
+  int stages;
+  uint32_t stage_bytes;  // K area + V area + Q area
+  float scale_log2;
+  int partition_blocks;  // fixed mode when > 0
+  int max_splits;
+  int balanced_ctas;
+  DecodeWorkspace ws;
+  uint32_t* status;
+};
+
+struct Layout {
+  uint32_t barriers, meta, pbuf, sched, total;
+};
+
+__host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline Layout make_layout(int stages, uint32_t stage_bytes, int hpc, int g) {
+  Layout l;
+  uint32_t off = stages * stage_bytes;
+  l.barriers = off;
+  off += 2 * stages * 8;
+  l.meta = align_up(off, 16);
+  off = l.meta + stages * sizeof(StageMeta);
+  l.pbuf = align_up(off, 16);
+  off = l.pbuf + hpc * 2 * 16 * g * 4;
+  l.sched = align_up(off, 16);
+  off = l.sched + 64 * 8;
+  l.total = off;
+  return l;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ int load_ctx(const Params& p, int s, int bs) {
+  int c = p.context_lens[s];
+  const int cap = p.max_blocks * bs;
+  if (c < 0 || c > cap) {
+    report(p.status, TVL_DEV_BAD_CONTEXT_LEN);
+    c = c < 0 ? 0 : cap;
+  }
+  return c;
+}
+
+// Block-wide inclusive scan of one value per thread; every thread gets its
+// inclusive prefix and the block total.  All threads must call it.
+__device__ void block_scan(long long v, long long& incl, long long& total, long long* tmp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) tmp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    long long w = lane < nw ? tmp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(kFull, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < nw) tmp[lane] = w;
+  }
+  __syncthreads();
+  incl = x + (warp > 0 ? tmp[warp - 1] : 0);
+  total = tmp[nw - 1];
+  __syncthreads();
+}
+
+// First CTA of the balanced split whose block range [B*c/C, B*(c+1)/C)
+// contains flattened block x (the largest c with B*c/C <= x).
+__host__ __device__ inline long long balanced_cta_of(long long x, long long total, long long ctas) {
+  return ((x + 1) * ctas - 1) / total;
+}
+
+// Per-CTA schedule written to shared memory by the whole CTA.
+struct Schedule {
+  long long count;     // blocks to stream
+  int seq0;            // first sequence
+  int block0;          // first block inside it
+  int fixed_record;    // fixed mode: record of the single segment (-1: final)
+  int cta;             // balanced mode: CTA index inside the KV-head group
+};
+
+// ---------------------------------------------------------------- producer
+
+template <int G, int BS>
+__device__ void producer(const Params& p, const Schedule& sc, uint8_t* smem, const Layout& L) {
+  const int lane = threadIdx.x & 31;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.barriers);
+  uint64_t* empty = full + p.stages;
+  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + L.meta);
+  const int hg = blockIdx.z;
+  const int hpc = p.hpc;
+  const bool whole_rows = (hpc == p.hkv);
+  const uint32_t kv_bytes = BS * hpc * kRowBytes;
+  const uint32_t q_bytes = hpc * G * kRowBytes;
+  const uint64_t stream_policy = policy_evict_first();
+  const uint64_t keep_policy = policy_evict_last();
+  const bool fixed = p.partition_blocks > 0;
+
+  long long it = 0;
+  bool ok = true;
+
+  // Claims the next stage (waiting until its previous contents were used).
+  auto acquire = [&](int& st) -> bool {
+    st = static_cast<int>(it % p.stages);
+    bool good = true;
+    if (it >= p.stages && lane == 0)
+      good = mbar_wait(&empty[st], static_cast<uint32_t>(((it / p.stages) - 1) & 1));
+    return __shfl_sync(kFull, good ? 1 : 0, 0) != 0;
+  };
+
+  int s = sc.seq0;
+  long long b = sc.block0;
+  long long left = sc.count;
+  bool first_seg = true;
+  int win_base = -1000000;
+  int win_ctx = 0;
+  while (ok && left > 0 && s < p.num_seqs) {
+    if (s - win_base >= 32 || s < win_base) {
+      win_base = s;
+      win_ctx = (s + lane < p.num_seqs) ? load_ctx(p, s + lane, BS) : 0;
+    }
+    const int ctx = __shfl_sync(kFull, win_ctx, s - win_base);
+    const long long nb = (ctx + BS - 1) / BS;
+    if (b >= nb) {
+      ++s;
+      b = 0;
+      continue;
+    }
+    const long long e = (nb < b + left) ? nb : b + left;
+    int record;
+    if (fixed) {
+      record = sc.fixed_record;
+    } else {
+      record = (b == 0 && e == nb) ? -1 : 2 * sc.cta + (first_seg ? 0 : 1);
+    }
+    const int32_t* table = p.block_tables + static_cast<long long>(s) * p.max_blocks;
+    int tbl = 0;
+    for (long long blk = b; blk < e && ok; ++blk) {
+      const int slot = static_cast<int>((blk - b) & 31);
+      if (slot == 0) tbl = (blk + lane < e) ? table[blk + lane] : 0;
+      int phys = __shfl_sync(kFull, tbl, slot);
+      if (phys < 0 || phys >= p.num_blocks) {
+        if (lane == 0) report(p.status, TVL_DEV_BAD_BLOCK_ID);
+        phys = 0;
+      }
+      int st;
+      if (!acquire(st)) {
+        ok = false;
+        break;
+      }
+      const int flags = (blk == b ? kSegFirst : 0) | (blk == e - 1 ? kSegLast : 0);
+      uint8_t* kdst = smem + static_cast<size_t>(st) * p.stage_bytes;
+      uint8_t* vdst = kdst + kv_bytes;
+      uint8_t* qdst = vdst + kv_bytes;
+      if (lane == 0) {
+        StageMeta m;
+        m.seq = s;
+        const long long rem = ctx - blk * BS;
+        m.valid = static_cast<int>(rem < BS ? rem : BS);
+        m.flags = flags;
+        m.record = record;
+        meta[st] = m;
+        mbar_arrive_expect_tx(&full[st], 2 * kv_bytes + ((flags & kSegFirst) ? q_bytes : 0));
+      }
+      __syncwarp();
+      const long long tok0 = static_cast<long long>(phys) * BS;
+      if (whole_rows) {
+        if (lane == 0) {
+          const size_t off = static_cast<size_t>(tok0) * p.hkv * kD;
+          bulk_load(kdst, p.k_cache + off, kv_bytes, &full[st], stream_policy);
+          bulk_load(vdst, p.v_cache + off, kv_bytes, &full[st], stream_policy);
+        }
+      } else {
+        for (int t = lane; t < BS; t += 32) {
+          const size_t off = (static_cast<size_t>(tok0 + t) * p.hkv + hg * hpc) * kD;
+          bulk_load(kdst + t * hpc * kRowBytes, p.k_cache + off, hpc * kRowBytes, &full[st],
+                    stream_policy);
+          bulk_load(vdst + t * hpc * kRowBytes, p.v_cache + off, hpc * kRowBytes, &full[st],
+                    stream_policy);
+        }
+      }
+      if ((flags & kSegFirst) && lane == 1) {
+        const size_t off = (static_cast<size_t>(s) * p.hq + hg * hpc * G) * kD;
+        bulk_load(qdst, p.q + off, q_bytes, &full[st], keep_policy);
+      }
+      ++it;
+    }
+    left -= e - b;
+    first_seg = false;
+    ++s;
+    b = 0;
+  }
+  // Tell the consumers to stop.
+  int st;
+  if (ok && acquire(st)) {
+    if (lane == 0) {
+      meta[st].flags = kTerminate;
+      mbar_arrive(&full[st]);
+    }
+    ++it;
+  } else {
+    if (lane == 0) report(p.status, kDevTimeout);
+  }
+  // Copies still in flight must land before the CTA may exit.
+  if (lane == 0) {
+    for (int i = 0; i < p.stages; ++i) {
+      if (it <= i) break;
+      const long long last = i + ((it - 1 - i) / p.stages) * p.stages;   // last fill of stage i
+      if (!mbar_wait(&full[i], static_cast<uint32_t>((last / p.stages) & 1))) {
+        report(p.status, kDevTimeout);
+      }
+    }
+  }
+}
+
+// --------------------------------------------------------------- consumers
+
+template <int G>
+struct LaneMap {
+  // After the butterfly, lane c (0..7) of a token group holds kVals values
+  // with logical indices jbase + r, where j = 4 * head + token.
+  static constexpr int kVals = G >= 2 ? G / 2 : 1;
+  __device__ static int xor_mask(int c) { return G >= 2 ? c * (G / 2) : (c >> 1); }
+  __device__ static int jbase(int c) { return G >= 2 ? c * (G / 2) : (c >> 1); }
+  // dim-chunk lane c holding head h after the butterfly
+  __device__ static int src_c(int h) { return G >= 2 ? h * 8 / G : 0; }
+};
+
+template <int G>
+__device__ __forceinline__ float reduce_max_head(float x) {
+  x = fmaxf(x, __shfl_xor_sync(kFull, x, 8));
+  x = fmaxf(x, __shfl_xor_sync(kFull, x, 16));
+  if constexpr (G == 4) x = fmaxf(x, __shfl_xor_sync(kFull, x, 1));
+  if constexpr (G == 2) {
+    x = fmaxf(x, __shfl_xor_sync(kFull, x, 1));
+    x = fmaxf(x, __shfl_xor_sync(kFull, x, 2));
+  }
+  if constexpr (G == 1) {
+    x = fmaxf(x, __shfl_xor_sync(kFull, x, 2));
+    x = fmaxf(x, __shfl_xor_sync(kFull, x, 4));
+  }
+  return x;
+}
+
+template <int G>
+__device__ __forceinline__ float reduce_sum_head(float x) {
+  x += __shfl_xor_sync(kFull, x, 8);
+  x += __shfl_xor_sync(kFull, x, 16);
+  if constexpr (G == 4) x += __shfl_xor_sync(kFull, x, 1);
+  if constexpr (G == 2) {
+    x += __shfl_xor_sync(kFull, x, 1);
+    x += __shfl_xor_sync(kFull, x, 2);
+  }
+  if constexpr (G == 1) {   // only even dim-chunk lanes carry a (duplicated) value
+    x += __shfl_xor_sync(kFull, x, 1);
+    x += __shfl_xor_sync(kFull, x, 2);
+    x += __shfl_xor_sync(kFull, x, 4);
+  }
+  return x;
+}
+
+template <int G>
+struct ConsumerState {
+  float2 qf[G][4];    // q of head (hr ^ mh), dims 8c..8c+7, scaled by scale*log2e
+  float2 acc[G][4];   // unnormalised output of head h, dims 8c..8c+7 (this lane's tokens)
+  float m_used;       // reference maximum of this lane's head
+  float l_part;       // this lane's share of the softmax denominator
+};
+
+template <int G, bool kFullChunk>
+__device__ __forceinline__ void process_chunk(ConsumerState<G>& st, const uint8_t* kbase,
+                                              const uint8_t* vbase, int row0, int valid,
+                                              int hpc, int w, float* pbuf) {
+  using M = LaneMap<G>;
+  const int lane = threadIdx.x & 31;
+  const int c = lane & 7, tg = lane >> 3;
+  const int mi = M::xor_mask(c) & 3;
+  constexpr int N = 4 * G;
+
+  // --- scores: part[4*hr + ir] = q(head hr^mh) . k(token ir^mi) over 8 dims
+  float part[N];
+#pragma unroll
+  for (int ir = 0; ir < 4; ++ir) {
+    const int t = row0 + tg * 4 + (ir ^ mi);
+    const uint4 kw =
+        *reinterpret_cast<const uint4*>(kbase + (t * hpc + w) * kRowBytes + c * 16);
+    const float2 k0 = bf16x2_to_float2(kw.x), k1 = bf16x2_to_float2(kw.y);
+    const float2 k2 = bf16x2_to_float2(kw.z), k3 = bf16x2_to_float2(kw.w);
+#pragma unroll
+    for (int hr = 0; hr < G; ++hr) {
+      float2 a = __fmul2_rn(st.qf[hr][0], k0);
+      a = __ffma2_rn(st.qf[hr][1], k1, a);
+      a = __ffma2_rn(st.qf[hr][2], k2, a);
+      a = __ffma2_rn(st.qf[hr][3], k3, a);
+      part[4 * hr + ir] = a.x + a.y;
+    }
+  }
+  // --- transposing butterfly over the 8 dim-chunk lanes
+  if constexpr (G >= 2) {
+#pragma unroll
+    for (int k = 0; k < N / 2; ++k) part[k] += __shfl_xor_sync(kFull, part[k + N / 2], 4);
+#pragma unroll
+    for (int k = 0; k < N / 4; ++k) part[k] += __shfl_xor_sync(kFull, part[k + N / 4], 2);
+#pragma unroll
+    for (int k = 0; k < N / 8; ++k) part[k] += __shfl_xor_sync(kFull, part[k + N / 8], 1);
+  } else {
+    part[0] += __shfl_xor_sync(kFull, part[2], 4);
+    part[1] += __shfl_xor_sync(kFull, part[3], 4);
+    part[0] += __shfl_xor_sync(kFull, part[1], 2);
+    part[0] += __shfl_xor_sync(kFull, part[0], 1);
+  }
+  constexpr int R = M::kVals;
+  const int jb = M::jbase(c);
+  if constexpr (!kFullChunk) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int t = row0 + tg * 4 + ((jb + r) & 3);
+      if (t >= valid) part[r] = -INFINITY;
+    }
+  }
+  // --- online softmax (exp2 domain, lazily moved reference maximum)
+  float cm = part[0];
+#pragma unroll
+  for (int r = 1; r < R; ++r) cm = fmaxf(cm, part[r]);
+  cm = reduce_max_head<G>(cm);
+  if (__any_sync(kFull, cm > st.m_used + kRescaleLog2)) {
+    const float m_new = fmaxf(st.m_used, cm);
+    const float f = ex2(st.m_used - m_new);
+    st.m_used = m_new;
+    st.l_part *= f;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float fh = __shfl_sync(kFull, f, tg * 8 + M::src_c(h));
+      const float2 ff = make_float2(fh, fh);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) st.acc[h][k] = __fmul2_rn(st.acc[h][k], ff);
+    }
+  }
+  float pr[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    pr[r] = ex2(part[r] - st.m_used);
+    if (G > 1 || (c & 1) == 0) st.l_part += pr[r];
+  }
+  float* pb = pbuf + tg * N;
+  if constexpr (R == 4) {
+    *reinterpret_cast<float4*>(pb + jb) = make_float4(pr[0], pr[1], pr[2], pr[3]);
+  } else if constexpr (R == 2) {
+    *reinterpret_cast<float2*>(pb + jb) = make_float2(pr[0], pr[1]);
+  } else {
+    pb[jb] = pr[0];
+  }
+  __syncwarp();
+  // --- o += p . V
+  float4 ph[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) ph[h] = *reinterpret_cast<const float4*>(pb + 4 * h);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = row0 + tg * 4 + i;
+    uint4 vw = *reinterpret_cast<const uint4*>(vbase + (t * hpc + w) * kRowBytes + c * 16);
+    if constexpr (!kFullChunk) {
+      if (t >= valid) vw = make_uint4(0, 0, 0, 0);   // unused slots may hold anything
+    }
+    const float2 v0 = bf16x2_to_float2(vw.x), v1 = bf16x2_to_float2(vw.y);
+    const float2 v2 = bf16x2_to_float2(vw.z), v3 = bf16x2_to_float2(vw.w);
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float pv = i == 0 ? ph[h].x : i == 1 ? ph[h].y : i == 2 ? ph[h].z : ph[h].w;
+      const float2 pp = make_float2(pv, pv);
+      st.acc[h][0] = __ffma2_rn(pp, v0, st.acc[h][0]);
+      st.acc[h][1] = __ffma2_rn(pp, v1, st.acc[h][1]);
+      st.acc[h][2] = __ffma2_rn(pp, v2, st.acc[h][2]);
+      st.acc[h][3] = __ffma2_rn(pp, v3, st.acc[h][3]);
+    }
+  }
+}
+
+template <int G>
+__device__ __forceinline__ void finish_segment(ConsumerState<G>& st, const Params& p, int seq,
+                                               int record, int hq0) {
+  using M = LaneMap<G>;
+  const int lane = threadIdx.x & 31;
+  const int c = lane & 7, tg = lane >> 3;
+  const float lt = reduce_sum_head<G>(st.l_part);
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float2 a = st.acc[h][k];
+      a.x += __shfl_xor_sync(kFull, a.x, 8);
+      a.y += __shfl_xor_sync(kFull, a.y, 8);
+      a.x += __shfl_xor_sync(kFull, a.x, 16);
+      a.y += __shfl_xor_sync(kFull, a.y, 16);
+      st.acc[h][k] = a;
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const float lh = __shfl_sync(kFull, lt, tg * 8 + M::src_c(h));
+    const float mh = __shfl_sync(kFull, st.m_used, tg * 8 + M::src_c(h));
+    if ((h & 3) == tg) {
+      const long long row = static_cast<long long>(record < 0 ? seq : record) * p.hq + hq0 + h;
+      if (record < 0) {
+        const float inv = 1.0f / lh;
+        float4* dst = reinterpret_cast<float4*>(p.out + row * kD + c * 8);
+        dst[0] = make_float4(st.acc[h][0].x * inv, st.acc[h][0].y * inv, st.acc[h][1].x * inv,
+                             st.acc[h][1].y * inv);
+        dst[1] = make_float4(st.acc[h][2].x * inv, st.acc[h][2].y * inv, st.acc[h][3].x * inv,
+                             st.acc[h][3].y * inv);
+      } else {
+        float4* dst = reinterpret_cast<float4*>(p.ws.acc + row * kD + c * 8);
+        dst[0] = make_float4(st.acc[h][0].x, st.acc[h][0].y, st.acc[h][1].x, st.acc[h][1].y);
+        dst[1] = make_float4(st.acc[h][2].x, st.acc[h][2].y, st.acc[h][3].x, st.acc[h][3].y);
+        if (c == 0) {
+          p.ws.m[row] = mh;
+          p.ws.l[row] = lh;
+        }
+      }
+    }
+  }
+}
+
+template <int G, int BS>
+__device__ void consumer(const Params& p, uint8_t* smem, const Layout& L) {
+  using M = LaneMap<G>;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int c = lane & 7;
+  const int w = warp;
+  const int hpc = p.hpc;
+  const int kvh = blockIdx.z * hpc + w;
+  const int hq0 = kvh * G;
+  const int mh = M::xor_mask(c) >> 2;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.barriers);
+  uint64_t* empty = full + p.stages;
+  const StageMeta* meta = reinterpret_cast<const StageMeta*>(smem + L.meta);
+  float* pbuf_w = reinterpret_cast<float*>(smem + L.pbuf) + w * 2 * 16 * G;
+  const uint32_t kv_bytes = BS * hpc * kRowBytes;
+
+  ConsumerState<G> st;
+  st.m_used = -INFINITY;
+  st.l_part = 0.f;
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      st.acc[h][k] = make_float2(0.f, 0.f);
+      st.qf[h][k] = make_float2(0.f, 0.f);
+    }
+  int chunk_no = 0;
+  for (long long it = 0;; ++it) {
+    const int s = static_cast<int>(it % p.stages);
+    if (!mbar_wait(&full[s], static_cast<uint32_t>((it / p.stages) & 1))) {
+      if (lane == 0) report(p.status, kDevTimeout);
+      return;
+    }
+    const StageMeta md = meta[s];
+    if (md.flags & kTerminate) break;
+    const uint8_t* kbase = smem + static_cast<size_t>(s) * p.stage_bytes;
+    const uint8_t* vbase = kbase + kv_bytes;
+    if (md.flags & kSegFirst) {
+      const uint8_t* qbase = vbase + kv_bytes;
+      st.m_used = -INFINITY;
+      st.l_part = 0.f;
+#pragma unroll
+      for (int hr = 0; hr < G; ++hr) {
+        const uint4 qw = *reinterpret_cast<const uint4*>(qbase + (w * G + (hr ^ mh)) * kRowBytes +
+                                                         c * 16);
+        const float2 sl = make_float2(p.scale_log2, p.scale_log2);
+        st.qf[hr][0] = __fmul2_rn(bf16x2_to_float2(qw.x), sl);
+        st.qf[hr][1] = __fmul2_rn(bf16x2_to_float2(qw.y), sl);
+        st.qf[hr][2] = __fmul2_rn(bf16x2_to_float2(qw.z), sl);
+        st.qf[hr][3] = __fmul2_rn(bf16x2_to_float2(qw.w), sl);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) st.acc[hr][k] = make_float2(0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int ch = 0; ch < BS / kChunk; ++ch) {
+      const int row0 = ch * kChunk;
+      if (row0 < md.valid) {
+        float* pb = pbuf_w + (chunk_no & 1) * 16 * G;
+        if (md.valid >= row0 + kChunk)
+          process_chunk<G, true>(st, kbase, vbase, row0, md.valid, hpc, w, pb);
+        else
+          process_chunk<G, false>(st, kbase, vbase, row0, md.valid, hpc, w, pb);
+        ++chunk_no;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (md.flags & kSegLast) finish_segment<G>(st, p, md.seq, md.record, hq0);
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int G, int BS>
+__global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32, 1) decode_kernel(const Params p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const Layout L = make_layout(p.stages, p.stage_bytes, p.hpc, G);
+  Schedule* sched = reinterpret_cast<Schedule*>(smem + L.sched);
+  long long* tmp = reinterpret_cast<long long*>(smem + L.sched + 64);
+  const int tid = threadIdx.x;
+
+  if (tid == 0) {
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.barriers);
+    uint64_t* empty = full + p.stages;
+    for (int i = 0; i < p.stages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], p.hpc);
+    }
+    fence_barrier_init();
+  }
+
+  if (p.partition_blocks > 0) {
+    // fixed windows: CTA (x = window, y = sequence)
+    const int s = blockIdx.y;
+    const int win = blockIdx.x;
+    const int ctx = load_ctx(p, s, BS);
+    const long long nb = (ctx + BS - 1) / BS;
+    const long long b0 = static_cast<long long>(win) * p.partition_blocks;
+    if (tid == 0) {
+      const long long nsplit = (nb + p.partition_blocks - 1) / p.partition_blocks;
+      sched->seq0 = s;
+      sched->block0 = static_cast<int>(b0);
+      sched->count = b0 < nb ? ((nb - b0) < p.partition_blocks ? nb - b0 : p.partition_blocks) : 0;
+      sched->fixed_record = nsplit <= 1 ? -1 : s * p.max_splits + win;
+      sched->cta = win;
+    }
+    if (nb == 0 && win == 0) {   // empty context: zero output rows
+      const long long base = (static_cast<long long>(s) * p.hq + blockIdx.z * p.hpc * G) * kD;
+      for (int i = tid; i < p.hpc * G * kD; i += blockDim.x) p.out[base + i] = 0.f;
+    }
+  } else {
+    // balanced: this CTA streams flattened blocks [B*c/C, B*(c+1)/C)
+    const int cta = blockIdx.x;
+    long long total = 0;
+    for (int base = 0; base < p.num_seqs; base += blockDim.x) {
+      const int s = base + tid;
+      const long long nb = s < p.num_seqs ? (load_ctx(p, s, BS) + BS - 1) / BS : 0;
+      long long incl, chunk_total;
+      block_scan(nb, incl, chunk_total, tmp);
+      total += chunk_total;
+    }
+    const long long lo = total * cta / p.balanced_ctas;
+    const long long hi = total * (cta + 1) / p.balanced_ctas;
+    if (tid == 0) {
+      sched->count = hi - lo;
+      sched->seq0 = p.num_seqs;
+      sched->block0 = 0;
+      sched->fixed_record = -1;
+      sched->cta = cta;
+    }
+    __syncthreads();
+    long long run = 0;
+    if (hi > lo) {
+      for (int base = 0; base < p.num_seqs; base += blockDim.x) {
+        const int s = base + tid;
+        const long long nb = s < p.num_seqs ? (load_ctx(p, s, BS) + BS - 1) / BS : 0;
+        long long incl, chunk_total;
+        block_scan(nb, incl, chunk_total, tmp);
+        const long long excl = run + incl - nb;
+        if (nb > 0 && excl <= lo && lo < excl + nb) {
+          sched->seq0 = s;
+          sched->block0 = static_cast<int>(lo - excl);
+        }
+        run += chunk_total;
+      }
+    }
+  }
+  __syncthreads();
+  const Schedule sc = *sched;
+  if (static_cast<int>(threadIdx.x >> 5) == p.hpc) {
+    producer<G, BS>(p, sc, smem, L);
+  } else {
+    consumer<G, BS>(p, smem, L);
+  }
+}
+
+// ------------------------------------------------------------------- merge
+
+struct MergeParams {
+  float* out;
+  const int32_t* context_lens;
+  int num_seqs, hq, max_blocks, bs;
+  int partition_blocks, max_splits, balanced_ctas;
+  DecodeWorkspace ws;
+  uint32_t* status;
+};
+
+constexpr int kMergeWarps = 8;
+
+__device__ __forceinline__ int merge_ctx(const MergeParams& p, int s) {
+  int c = p.context_lens[s];
+  const int cap = p.max_blocks * p.bs;
+  return c < 0 ? 0 : (c > cap ? cap : c);
+}
+
+// Combines the partial records of one sequence:
+//   M = max_r m_r;  out = sum_r 2^(m_r - M) acc_r / sum_r 2^(m_r - M) l_r.
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeParams p) {
+  __shared__ long long tmp[32];
+  const int s = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int h = blockIdx.y * kMergeWarps + warp;
+  const long long nb = (merge_ctx(p, s) + p.bs - 1) / p.bs;
+
+  long long first = 0, count = 0;    // fixed mode record list
+  long long seq_start = 0, total = 0, c_first = 0, c_last = -1;
+  const bool fixed = p.partition_blocks > 0;
+  if (fixed) {
+    if (nb <= p.partition_blocks) return;   // single window: decode wrote the output
+    first = static_cast<long long>(s) * p.max_splits;
+    count = (nb + p.partition_blocks - 1) / p.partition_blocks;
+  } else {
+    if (nb == 0) {
+      if (h < p.hq) {
+        float* dst = p.out + (static_cast<long long>(s) * p.hq + h) * kD;
+        dst[lane] = 0.f;
+        dst[lane + 32] = 0.f;
+      }
+      return;
+    }
+    long long tot_part = 0, pre_part = 0;
+    for (int i = tid; i < p.num_seqs; i += blockDim.x) {
+      const long long n = (merge_ctx(p, i) + p.bs - 1) / p.bs;
+      tot_part += n;
+      if (i < s) pre_part += n;
+    }
+    long long incl, all;
+    block_scan(tot_part, incl, all, tmp);
+    total = all;
+    block_scan(pre_part, incl, all, tmp);
+    seq_start = all;
+    const long long C = p.balanced_ctas;
+    c_first = balanced_cta_of(seq_start, total, C);
+    c_last = balanced_cta_of(seq_start + nb - 1, total, C);
+    if (c_first == c_last) return;   // one CTA held the whole sequence
+  }
+  if (h >= p.hq) return;
+
+  // record index of the k-th candidate, or -1 when that CTA holds none of s
+  auto record_of = [&](long long k) -> long long {
+    if (fixed) return first + k;
+    const long long c = c_first + k;
+    const long long lo = total * c / p.balanced_ctas;
+    const long long hi = total * (c + 1) / p.balanced_ctas;
+    const long long a = lo > seq_start ? lo : seq_start;
+    const long long b = hi < seq_start + nb ? hi : seq_start + nb;
+    if (a >= b) return -1;
+    return 2 * c + (seq_start <= lo ? 0 : 1);
+  };
+  const long long n_cand = fixed ? count : (c_last - c_first + 1);
+
+  float mx = -INFINITY;
+  for (long long k = lane; k < n_cand; k += 32) {
+    const long long r = record_of(k);
+    if (r >= 0) mx = fmaxf(mx, p.ws.m[r * p.hq + h]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+  float den = 0.f, o0 = 0.f, o1 = 0.f;
+  for (long long k = 0; k < n_cand; ++k) {
+    const long long r = record_of(k);
+    if (r < 0) continue;
+    const long long row = r * p.hq + h;
+    const float wgt = ex2(p.ws.m[row] - mx);
+    den += wgt * p.ws.l[row];
+    o0 += wgt * p.ws.acc[row * kD + lane];
+    o1 += wgt * p.ws.acc[row * kD + lane + 32];
+  }
+  const float inv = 1.0f / den;
+  float* dst = p.out + (static_cast<long long>(s) * p.hq + h) * kD;
+  dst[lane] = o0 * inv;
+  dst[lane + 32] = o1 * inv;
+}
+
+template <int G, int BS>
+cudaError_t launch_t(const Params& prm, dim3 grid, uint32_t smem_bytes, cudaStream_t stream) {
+  auto kern = decode_kernel<G, BS>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, (prm.hpc + 1) * 32, smem_bytes, stream>>>(prm);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+long long decode_records(int num_seqs, int max_blocks_per_seq, int partition_blocks,
+                         int balanced_ctas) {
+  if (partition_blocks > 0) {
+    const long long splits = (max_blocks_per_seq + partition_blocks - 1) / partition_blocks;
+    return splits <= 1 ? 0 : static_cast<long long>(num_seqs) * splits;
+  }
+  return 2LL * balanced_ctas;
+}
+
+size_t decode_workspace_bytes(long long records, int num_q_heads, int head_dim) {
+  if (records <= 0) return 0;
+  const size_t rows = static_cast<size_t>(records) * num_q_heads;
+  const size_t a = (rows * sizeof(float) + 255) / 256 * 256;
+  return 2 * a + rows * head_dim * sizeof(float);
+}
+
+DecodeWorkspace decode_workspace_carve(void* base, long long records, int num_q_heads,
+                                       int head_dim) {
+  DecodeWorkspace ws{nullptr, nullptr, nullptr};
+  if (records <= 0 || base == nullptr) return ws;
+  const size_t rows = static_cast<size_t>(records) * num_q_heads;
+  const size_t a = (rows * sizeof(float) + 255) / 256 * 256;
+  uint8_t* b = static_cast<uint8_t*>(base);
+  ws.m = reinterpret_cast<float*>(b);
+  ws.l = reinterpret_cast<float*>(b + a);
+  ws.acc = reinterpret_cast<float*>(b + 2 * a);
+  (void)head_dim;
+  return ws;
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.num_seqs == 0) return cudaSuccess;
+  const int G = a.num_q_heads / a.num_kv_heads;
+  const int hpc = a.num_kv_heads < kMaxHeadsPerCta ? a.num_kv_heads : kMaxHeadsPerCta;
+  const int groups = a.num_kv_heads / hpc;
+  const int bs = a.block_size;
+
+  Params prm;
+  prm.out = a.out;
+  prm.q = static_cast<const __nv_bfloat16*>(a.q);
+  prm.k_cache = static_cast<const __nv_bfloat16*>(a.k_cache);
+  prm.v_cache = static_cast<const __nv_bfloat16*>(a.v_cache);
+  prm.block_tables = a.block_tables;
+  prm.context_lens = a.context_lens;
+  prm.num_seqs = a.num_seqs;
+  prm.hq = a.num_q_heads;
+  prm.hkv = a.num_kv_heads;
+  prm.num_blocks = a.num_blocks;
+  prm.max_blocks = a.max_blocks_per_seq;
+  prm.hpc = hpc;
+  prm.stage_bytes = align_up(2 * bs * hpc * kRowBytes + hpc * G * kRowBytes, 128);
+  const uint32_t fixed_part = make_layout(0, prm.stage_bytes, hpc, G).total + 2 * 8 * 8 + 16 * 8;
+  int stages = static_cast<int>((kSmemBudget - fixed_part) / prm.stage_bytes);
+  stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
+  prm.stages = stages;
+  prm.scale_log2 = a.scale * kLog2e;
+  prm.partition_blocks = a.partition_blocks;
+  prm.max_splits = a.max_splits;
+  prm.balanced_ctas = a.balanced_ctas;
+  prm.ws = a.ws;
+  prm.status = a.status;
+  const uint32_t smem = make_layout(stages, prm.stage_bytes, hpc, G).total;
+
+  dim3 grid;
+  if (a.partition_blocks > 0)
+    grid = dim3(a.max_splits, a.num_seqs, groups);
+  else
+    grid = dim3(a.balanced_ctas, 1, groups);
+
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (G * 100 + bs) {
+    case 116: e = launch_t<1, 16>(prm, grid, smem, stream); break;
+    case 132: e = launch_t<1, 32>(prm, grid, smem, stream); break;
+    case 216: e = launch_t<2, 16>(prm, grid, smem, stream); break;
+    case 232: e = launch_t<2, 32>(prm, grid, smem, stream); break;
+    case 416: e = launch_t<4, 16>(prm, grid, smem, stream); break;
+    case 432: e = launch_t<4, 32>(prm, grid, smem, stream); break;
+    case 816: e = launch_t<8, 16>(prm, grid, smem, stream); break;
+    case 832: e = launch_t<8, 32>(prm, grid, smem, stream); break;
+    default: return cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess) return e;
+
+  const bool need_merge =
+      a.partition_blocks == 0 ||
+      (a.max_blocks_per_seq + a.partition_blocks - 1) / a.partition_blocks > 1;
+  if (!need_merge) return cudaSuccess;
+  MergeParams mp;
+  mp.out = a.out;
+  mp.context_lens = a.context_lens;
+  mp.num_seqs = a.num_seqs;
+  mp.hq = a.num_q_heads;
+  mp.max_blocks = a.max_blocks_per_seq;
+  mp.bs = bs;
+  mp.partition_blocks = a.partition_blocks;
+  mp.max_splits = a.max_splits;
+  mp.balanced_ctas = a.balanced_ctas;
+  mp.ws = a.ws;
+  mp.status = a.status;
+  dim3 mgrid(a.num_seqs, (a.num_q_heads + kMergeWarps - 1) / kMergeWarps);
+  merge_kernel<<<mgrid, kMergeWarps * 32, 0, stream>>>(mp);
+  return cudaGetLastError();
+}
+
+}  // namespace tvl

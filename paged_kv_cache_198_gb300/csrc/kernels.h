@@ -1,0 +1,75 @@
+// kernels.h -- internal interface between the C ABI (api.cu) and the kernel
+// translation units.  Arguments arrive here already validated.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace tvl {
+
+struct KvWriteArgs {
+  const void* k_new;
+  const void* v_new;
+  void* k_cache;
+  void* v_cache;
+  const int32_t* slot_mapping;
+  int num_tokens;
+  int row_bytes;          // Hkv * D * 2, a multiple of 16
+  long long num_slots;    // NB * bs
+  uint32_t* status;
+};
+cudaError_t launch_kv_write(const KvWriteArgs& a, cudaStream_t stream);
+
+// Partial results of the decode (split-K) live in a workspace of `records`
+// records; record r, query head h: m (log2 domain running max used),
+// l (sum of exp2), acc[D] (unnormalised weighted sum of V).
+struct DecodeWorkspace {
+  float* m;     // [records, Hq]
+  float* l;     // [records, Hq]
+  float* acc;   // [records, Hq, D]
+};
+
+struct DecodeArgs {
+  float* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
+  int num_blocks, max_blocks_per_seq;
+  float scale;
+  int partition_blocks;   // > 0: fixed windows of this many blocks; 0: balanced
+  int max_splits;         // fixed mode: ceil(MB / partition_blocks)
+  int balanced_ctas;      // balanced mode: CTAs per KV-head group
+  DecodeWorkspace ws;
+  uint32_t* status;
+};
+
+// Number of workspace records the decode needs (0 = none).
+long long decode_records(int num_seqs, int max_blocks_per_seq, int partition_blocks,
+                         int balanced_ctas);
+// Byte layout of the workspace for `records` records.
+size_t decode_workspace_bytes(long long records, int num_q_heads, int head_dim);
+DecodeWorkspace decode_workspace_carve(void* base, long long records, int num_q_heads,
+                                       int head_dim);
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+struct PrefillArgs {
+  float* out;
+  const void* q;
+  const int32_t* query_start_loc;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int num_seqs, total_q_tokens, max_q_len, num_q_heads, num_kv_heads, head_dim;
+  int block_size, num_blocks, max_blocks_per_seq;
+  float scale;
+  uint32_t* status;
+};
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+
+}  // namespace tvl

@@ -1,0 +1,59 @@
+// kv_write.cu -- the slot-mapped paged KV write.
+//
+// [tiny-vllm README, curriculum "Paged KV cache"]: each new token's K and V
+// rows (Hkv * D bf16 values) are stored at the cache slot the host's block
+// allocator chose for it; slot = physical block * bs + offset indexes a row
+// of the flat [NB * bs, Hkv * D] view of the cache.
+//
+// One warp moves one token: its K row and its V row, with 16-byte vector
+// loads and stores (a 1 KB row is two 16-byte vectors per lane per tensor).
+// The work is a pure copy, bound by HBM bandwidth for large batches and by
+// launch latency for small ones.
+#include "device.cuh"
+#include "kernels.h"
+
+namespace tvl {
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    kv_write_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                    uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                    const int32_t* __restrict__ slot_mapping, int num_tokens, int row_vecs,
+                    long long num_slots, uint32_t* status) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long t = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + warp;
+  if (t >= num_tokens) return;
+  const long long slot = slot_mapping[t];
+  if (slot < 0) return;                      // padding token: nothing to store
+  if (slot >= num_slots) {                   // outside the pool: refuse, report
+    if (lane == 0) report(status, TVL_DEV_BAD_SLOT);
+    return;
+  }
+  const uint4* ks = k_new + t * row_vecs;
+  const uint4* vs = v_new + t * row_vecs;
+  uint4* kd = k_cache + slot * row_vecs;
+  uint4* vd = v_cache + slot * row_vecs;
+  for (int i = lane; i < row_vecs; i += 32) {
+    const uint4 kv = __ldcs(ks + i);         // read once: streaming
+    const uint4 vv = __ldcs(vs + i);
+    kd[i] = kv;
+    vd[i] = vv;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_write(const KvWriteArgs& a, cudaStream_t stream) {
+  if (a.num_tokens == 0) return cudaSuccess;
+  const int blocks = (a.num_tokens + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  kv_write_kernel<<<blocks, kWarpsPerBlock * 32, 0, stream>>>(
+      static_cast<const uint4*>(a.k_new), static_cast<const uint4*>(a.v_new),
+      static_cast<uint4*>(a.k_cache), static_cast<uint4*>(a.v_cache), a.slot_mapping,
+      a.num_tokens, a.row_bytes / 16, a.num_slots, a.status);
+  return cudaGetLastError();
+}
+
+}  // namespace tvl
