@@ -1,0 +1,426 @@
+"""Benchmark of the paged-attention hot path on GB300.
+
+Default: the Llama-3.2-1B-shaped single-layer decode step (64 sequences, 32
+query / 8 KV heads, head_dim 64, block_size 16, context ~ U{512..4096},
+blocks scattered over a 1.5x pool).  One step = the paged KV write of the
+batch's 64 new tokens + PagedAttention decode (balanced split-K + merge).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+                  [--config NAME]
+
+Prints one JSON line.  `value` is achieved HBM GB/s of the step's algorithmic
+bytes (each cached K/V byte counted once, plus q, out, the written rows and
+the metadata) over the device-timed step; `seq_steps_per_s` is sequences
+decoded per second.  The reference arm (`--impl reference`) times the CPU
+oracle on the host cores on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from paged_kv_cache_198_gb300 import workloads as W  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+CSRC = os.path.join(ROOT, "paged_kv_cache_198_gb300", "csrc")
+
+
+# ------------------------------------------------------------------ helpers
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(
+            d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(profile_name, files):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    try:
+        kv = {}
+        with open(path) as fh:
+            for line in fh:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("source_sha256") != source_sha(files):
+            return None
+        return int(float(kv["traffic_bytes_per_launch"]))
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- workloads
+
+
+def decode_algorithmic_bytes(wl):
+    s, hq, d = wl.q.shape
+    nblk = [(int(c) + wl.block_size - 1) // wl.block_size for c in wl.context_lens.tolist()]
+    return (wl.kv_bytes() + s * hq * d * 2 + s * hq * d * 4 + 4 * sum(nblk) + 4 * s)
+
+
+def write_algorithmic_bytes(wl):
+    t = int(wl.slot_mapping.numel())
+    return 2 * 2 * t * wl.num_kv_heads * wl.head_dim + 4 * t   # read new + write cache
+
+
+def prefill_flops(wl):
+    return 4.0 * wl.head_dim * wl.num_q_heads * wl.causal_pairs()
+
+
+# ------------------------------------------------------------ native decode
+
+
+def bench_decode(wl, args, rank, world, device):
+    import paged_kv_cache_198_gb300 as tvl
+
+    part = wl.partition_size
+    copies = max(1, math.ceil(3 * L2_BYTES / max(1, wl.kv_bytes())) + 1)
+    copies = min(copies, 4)
+    base = W.to_device(wl, device)
+    sets = [base]
+    for _ in range(copies - 1):
+        sets.append({k: (v.clone() if k in ("k_cache", "v_cache") else v)
+                     for k, v in base.items()})
+    s, hq, d = wl.q.shape
+    out = torch.empty(s, hq, d, dtype=torch.float32, device=device)
+    ws_bytes = tvl.paged_attention_decode_workspace_size(
+        s, hq, wl.num_kv_heads, d, wl.max_blocks_per_seq, wl.block_size, part)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(t, ev=None):
+        tvl.paged_kv_write(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["slot_mapping"])
+        if ev is not None:
+            ev[0].record(stream)
+        tvl.paged_attention_decode(out, t["q"], t["k_cache"], t["v_cache"], t["block_tables"],
+                                   t["context_lens"], wl.scale, partition_size=part,
+                                   workspace=ws)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for i in range(args.warmup):
+        step(sets[i % copies])
+    torch.cuda.synchronize(device)
+    if tvl.get_device_status() != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    with ClockSampler(device.index if device.index is not None else 0) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            step(sets[i % copies], evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize(device)
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    dec_ms = [a.elapsed_time(b) for a, b in evs]
+
+    # end to end through the public API: H2D of the step's inputs from pinned
+    # host memory, the two calls, D2H of the output
+    host = {k: v.pin_memory() for k, v in
+            W.to_device(wl, "cpu").items() if k in ("q", "k_new", "v_new", "slot_mapping",
+                                                     "block_tables", "context_lens")}
+    out_host = torch.empty(s, hq, d, dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    dev_in = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+
+    def e2e_step(t):
+        for k, v in host.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        tvl.paged_kv_write(dev_in["k_new"], dev_in["v_new"], t["k_cache"], t["v_cache"],
+                           dev_in["slot_mapping"])
+        tvl.paged_attention_decode(out, dev_in["q"], t["k_cache"], t["v_cache"],
+                                   dev_in["block_tables"], dev_in["context_lens"], wl.scale,
+                                   partition_size=part, workspace=ws)
+        out_host.copy_(out, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(sets[i % copies])
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(sets[i % copies])
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = e0.elapsed_time(e1)
+    if tvl.get_device_status() != 0:
+        raise RuntimeError("device status word set during timing")
+    return {
+        "elapsed_ms": elapsed_ms, "decode_ms": statistics.mean(dec_ms),
+        "decode_ms_median": statistics.median(dec_ms), "e2e_ms": e2e_ms,
+        "h2d": h2d, "d2h": d2h, "copies": copies, "clocks": clocks.summary(),
+        "launches_per_step": 3 if (part == 0 or wl.max_blocks_per_seq * wl.block_size > part)
+        else 2,
+    }
+
+
+def cpu_baseline_decode(wl, budget_s=10.0):
+    """The oracle (write + decode of the whole batch) on the host cores,
+    repeated until about budget_s seconds have passed."""
+    import oracle
+
+    oracle.build()
+    cores = oracle.max_threads()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        kc, vc = oracle.kv_write(wl.k_cache, wl.v_cache, wl.k_new, wl.v_new, wl.slot_mapping)
+        oracle.decode(wl.q, kc, vc, wl.block_tables, wl.context_lens, wl.scale)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    per_step = (time.perf_counter() - t0) / reps
+    return per_step, cores, reps
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return os.uname().machine
+
+
+# -------------------------------------------------------------------- main
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--config", default="llama1b_decode",
+                    choices=["llama1b_decode", "continuous_batch", "long_splitk", "tiny"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    hbm_peak, bf16_peak, bf16_sus, peak_src = peaks()
+    metric = "paged-attn decode achieved HBM GB/s (% of GB300 peak); seq-steps/sec"
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        wl = W.named(args.config, 0)
+        import oracle
+
+        oracle.build()
+        for _ in range(args.warmup if args.warmup <= 3 else 3):
+            pass
+        step_bytes = decode_algorithmic_bytes(wl) + write_algorithmic_bytes(wl)
+        times = []
+        for i in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            kc, vc = oracle.kv_write(wl.k_cache, wl.v_cache, wl.k_new, wl.v_new,
+                                     wl.slot_mapping)
+            oracle.decode(wl.q, kc, vc, wl.block_tables, wl.context_lens, wl.scale)
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        per = sum(times) / len(times)
+        val = step_bytes / per / 1e9
+        line = {
+            "impl": "reference", "metric": metric, "value": round(val, 3), "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(per * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "seq_steps_per_s": round(wl.num_seqs / per, 1),
+            "config": {"workload": wl.name, "num_seqs": wl.num_seqs,
+                       "heads": f"{wl.num_q_heads}/{wl.num_kv_heads}",
+                       "head_dim": wl.head_dim, "block_size": wl.block_size,
+                       "partition_size": wl.partition_size},
+            "cpu_baseline": {"value": round(val, 3), "unit": "GB/s",
+                             "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": "the whole workload (paged write + decode of every "
+                                       "sequence) per step; " + cpu_model()},
+            "e2e": {"value": round(val, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from paged_kv_cache_198_gb300 import _build
+
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        torch.distributed.barrier()
+
+    wl = W.named(args.config, rank)        # every rank decodes its own batch
+    r = bench_decode(wl, args, rank, world, device)
+    step_bytes = decode_algorithmic_bytes(wl) + write_algorithmic_bytes(wl)
+    elapsed = torch.tensor([r["elapsed_ms"], r["e2e_ms"]], dtype=torch.float64, device=device)
+    units = torch.tensor([float(step_bytes), float(wl.num_seqs)], dtype=torch.float64,
+                         device=device)
+    if world > 1:
+        torch.distributed.all_reduce(elapsed, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.all_reduce(units, op=torch.distributed.ReduceOp.SUM)
+    if rank != 0:
+        torch.distributed.destroy_process_group()
+        return
+    t_ms, e2e_ms = float(elapsed[0]), float(elapsed[1])
+    total_bytes, total_seqs = float(units[0]), float(units[1])
+    per_step_ms = t_ms / args.steps
+    value = total_bytes * args.steps / (t_ms / 1e3) / 1e9
+    e2e_val = total_bytes * args.steps / (e2e_ms / 1e3) / 1e9
+
+    dec_bytes = decode_algorithmic_bytes(wl)
+    achieved = dec_bytes / (r["decode_ms"] / 1e3) / 1e9
+    traffic = recorded_traffic("decode_llama1b_decode.txt", ["decode.cu", "device.cuh"])
+    line = {
+        "metric": metric, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "seq_steps_per_s": round(total_seqs * args.steps / (t_ms / 1e3), 1),
+        "config": {
+            "workload": wl.name, "num_seqs": wl.num_seqs,
+            "heads": f"{wl.num_q_heads}/{wl.num_kv_heads}", "head_dim": wl.head_dim,
+            "block_size": wl.block_size, "num_blocks": wl.num_blocks,
+            "context_tokens": int(wl.context_lens.sum()),
+            "partition_size": wl.partition_size,
+            "step": "paged KV write of the new tokens + paged decode (+ split-K merge)",
+            "bytes_per_step": step_bytes,
+            "l2": f"inputs larger than L2: {r['copies']} rotating cache copies, "
+                  f"{wl.kv_bytes() / 1e6:.0f} MB K/V read per step vs 129 MB L2",
+        },
+        "roofline": {
+            "kernel": "decode (decode_kernel + merge_kernel, one C-ABI call)",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+            else "fallback 6.8 TB/s",
+            "algorithmic_bytes_per_launch": dec_bytes,
+            "launch_ms_mean": round(r["decode_ms"], 5),
+            "launch_ms_median": round(r["decode_ms_median"], 5),
+        },
+        "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"], "ms_per_step": round(e2e_ms / args.steps, 4)},
+        "gpu_launches": r["launches_per_step"] * args.steps,
+        "clocks": r["clocks"],
+    }
+    if not args.no_cpu_baseline and world == 1:
+        per, cores, reps = cpu_baseline_decode(wl)
+        line["cpu_baseline"] = {
+            "value": round(step_bytes / per / 1e9, 3), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{reps} full steps (paged write + fp64 decode of all {wl.num_seqs} "
+                      f"sequences), {per:.3f} s each; {cpu_model()}"}
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,134 @@
+"""GPU parity of the tcgen05 chunked causal prefill against the CPU oracle,
+plus the causal and placement invariants."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_198_gb300 as tvl
+from paged_kv_cache_198_gb300 import workloads as W
+from gpu_common import DEV, assert_clean_status, assert_close, oracle_caches
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_prefill(wl, write=True, tensors=None):
+    t = tensors if tensors is not None else W.to_device(wl, DEV)
+    if write:
+        tvl.paged_kv_write(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["slot_mapping"])
+    out = torch.full(tuple(wl.q.shape), float("nan"), dtype=torch.float32, device=DEV)
+    tvl.paged_attention_prefill(out, t["q"], t["query_start_loc"], t["k_cache"], t["v_cache"],
+                                t["block_tables"], t["context_lens"], wl.scale, wl.max_q_len)
+    torch.cuda.synchronize()
+    return out.double().cpu().numpy(), t
+
+
+def oracle_prefill(wl, write=True, row_mask=None):
+    kc, vc = oracle_caches(wl, write)
+    return oracle.prefill(wl.q, wl.query_start_loc, kc, vc, wl.block_tables, wl.context_lens,
+                          wl.scale, row_mask=row_mask)
+
+
+CASES = [
+    # (prefix lens, q lens, Hq, Hkv, bs)
+    ([0], [1], 4, 1, 16),
+    ([0], [100], 4, 2, 16),              # one partial tile, causal from row 0
+    ([0, 0], [128, 129], 8, 2, 16),      # exact tile and one row over
+    ([5, 300, 47], [20, 64, 200], 8, 2, 16),
+    ([130, 0, 1000], [1, 255, 77], 32, 8, 32),
+    ([17, 2000], [300, 3], 8, 1, 64),    # G = 8
+    ([64, 0], [70, 33], 4, 4, 128),      # G = 1, block = one whole KV tile
+    ([1, 2, 3, 129, 257], [128, 127, 129, 1, 2], 16, 8, 16),
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_prefill_random_shapes(case):
+    prefix, lq, hq, hkv, bs = CASES[case]
+    wl = W.make_prefill(700 + case, prefix, lq, num_q_heads=hq, num_kv_heads=hkv, block_size=bs)
+    got, _ = gpu_prefill(wl)
+    assert_close(got, oracle_prefill(wl), f"case {case}")
+    assert_clean_status()
+
+
+@pytest.mark.parametrize("replica", [0, 1, 2])
+def test_prefill_chunked_config_sampled(replica):
+    wl = W.named("chunked_prefill", replica)
+    got, _ = gpu_prefill(wl)
+    gen = np.random.default_rng(replica)
+    mask = np.zeros(wl.total_q, dtype=np.uint8)
+    mask[gen.choice(wl.total_q, size=768, replace=False)] = 1
+    mask[int(wl.query_start_loc[0]):int(wl.query_start_loc[1])] = 1   # all of sequence 0
+    ref = oracle_prefill(wl, row_mask=mask)
+    assert_close(got, ref, f"chunked r{replica}")
+    assert np.isfinite(got).all()
+    assert_clean_status()
+
+
+def test_prefill_short_rows_with_large_values():
+    """Rows with one to a few visible keys and |v| ~ 8: the fp16 P.V path
+    must still meet the tolerance."""
+    wl = W.make_prefill(720, [0, 0], [8, 130], num_q_heads=8, num_kv_heads=2, block_size=16)
+    wl.k_new = (wl.k_new.float() * 3).to(torch.bfloat16)
+    wl.v_new = (wl.v_new.float() * 8).to(torch.bfloat16)
+    got, _ = gpu_prefill(wl)
+    assert_close(got, oracle_prefill(wl), "short rows")
+
+
+def test_prefill_poisoned_unused_slots():
+    wl = W.make_prefill(721, [3, 40, 200], [10, 100, 60], num_q_heads=8, num_kv_heads=2,
+                        block_size=32)
+    W.poison_unused(wl, 1.0e4)
+    got, _ = gpu_prefill(wl)
+    assert_close(got, oracle_prefill(wl), "poisoned")
+
+
+def test_prefill_bit_identical_under_block_permutation():
+    wl = W.make_prefill(722, [100, 700], [200, 129], num_q_heads=8, num_kv_heads=2,
+                        block_size=16)
+    base, t = gpu_prefill(wl)
+    kc = t["k_cache"].cpu()
+    vc = t["v_cache"].cpu()
+    gen = torch.Generator().manual_seed(5)
+    perm = torch.randperm(wl.num_blocks, generator=gen)
+    kc2 = torch.empty_like(kc)
+    vc2 = torch.empty_like(vc)
+    kc2[perm] = kc
+    vc2[perm] = vc
+    t2 = wl.block_tables.clone()
+    valid = t2 >= 0
+    t2[valid] = perm[t2[valid].long()].to(torch.int32)
+    wl.k_cache, wl.v_cache, wl.block_tables = kc2, vc2, t2
+    moved, _ = gpu_prefill(wl, write=False)
+    assert np.array_equal(base, moved)
+
+
+def test_prefill_causal_rows_ignore_later_keys():
+    wl = W.make_prefill(723, [50], [200], num_q_heads=4, num_kv_heads=1, block_size=16)
+    base, t = gpu_prefill(wl)
+    i = 90                                    # row 90 sits at position 140
+    pos = 50 + i
+    kc = t["k_cache"]
+    vc = t["v_cache"]
+    for j in range(pos + 1, 250):
+        b, o = int(wl.block_tables[0, j // 16]), j % 16
+        kc[b, o] = 5.0
+        vc[b, o] = -5.0
+    out = torch.full(tuple(wl.q.shape), float("nan"), dtype=torch.float32, device=DEV)
+    tvl.paged_attention_prefill(out, t["q"], t["query_start_loc"], kc, vc, t["block_tables"],
+                                t["context_lens"], wl.scale, wl.max_q_len)
+    pert = out.double().cpu().numpy()
+    assert np.array_equal(base[:i + 1], pert[:i + 1])
+    assert not np.array_equal(base[i + 1], pert[i + 1])
+
+
+def test_prefill_matches_decode_for_single_token_chunks():
+    """A prefill chunk of one token per sequence is a decode step."""
+    wl = W.make_prefill(724, [33, 500, 1], [1, 1, 1], num_q_heads=32, num_kv_heads=8,
+                        block_size=16)
+    got, t = gpu_prefill(wl)
+    out = torch.empty(tuple(wl.q.shape), dtype=torch.float32, device=DEV)
+    tvl.paged_attention_decode(out, t["q"], t["k_cache"], t["v_cache"], t["block_tables"],
+                               t["context_lens"], wl.scale, partition_size=0)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(got, out.double().cpu().numpy(), rtol=0, atol=2e-3)
