@@ -81,9 +81,9 @@ def recorded_traffic(profile_name, files):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -97,7 +97,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -119,13 +119,24 @@ class ClockSampler:
             if self.thread:
                 self.thread.join(timeout=2)
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and active throttle reasons of the samples taken
+        between host times t0 and t1 (all samples when not given)."""
+        import datetime
+
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
+            if t0 is not None:
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    continue
+                if not (t0 <= ts <= t1):
+                    continue
             try:
                 sm.append(float(parts[1]))
                 mx.append(float(parts[2]))
@@ -138,6 +149,22 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def combine_ranks(times_ms, units, world, device):
+    """Whole-job view of a weak-scaling run: the slowest rank's times (MAX)
+    and the units every rank processed (SUM).  Identity when world == 1."""
+    t = torch.tensor([float(x) for x in times_ms], dtype=torch.float64, device=device)
+    u = torch.tensor([float(x) for x in units], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.all_reduce(u, op=torch.distributed.ReduceOp.SUM)
+    return [float(x) for x in t.tolist()], [float(x) for x in u.tolist()]
+
+
+def rank_workload(name, rank):
+    """Each rank decodes its own independent batch (replica seed = rank)."""
+    return W.named(name, rank)
 
 
 # --------------------------------------------------------------- workloads
@@ -203,11 +230,18 @@ def bench_decode(wl, args, rank, world, device):
         torch.distributed.barrier()
     torch.cuda.synchronize(device)
     with ClockSampler(device.index if device.index is not None else 0) as clocks:
+        time.sleep(0.5)                     # let the sampler start
+        for i in range(args.warmup):
+            step(sets[i % copies])
+        torch.cuda.synchronize(device)
+        host_t0 = time.time()
         start.record(stream)
         for i in range(args.steps):
             step(sets[i % copies], evs[i])
         stop.record(stream)
         torch.cuda.synchronize(device)
+        host_t1 = time.time()
+        time.sleep(0.1)
     if world > 1:
         torch.distributed.barrier()
     elapsed_ms = start.elapsed_time(stop)
@@ -249,7 +283,7 @@ def bench_decode(wl, args, rank, world, device):
     return {
         "elapsed_ms": elapsed_ms, "decode_ms": statistics.mean(dec_ms),
         "decode_ms_median": statistics.median(dec_ms), "e2e_ms": e2e_ms,
-        "h2d": h2d, "d2h": d2h, "copies": copies, "clocks": clocks.summary(),
+        "h2d": h2d, "d2h": d2h, "copies": copies, "clocks": clocks.summary(host_t0, host_t1),
         "launches_per_step": 3 if (part == 0 or wl.max_blocks_per_seq * wl.block_size > part)
         else 2,
     }
@@ -290,7 +324,7 @@ def cpu_model():
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--config", default="llama1b_decode",
@@ -357,20 +391,14 @@ def main():
     if world > 1:
         torch.distributed.barrier()
 
-    wl = W.named(args.config, rank)        # every rank decodes its own batch
+    wl = rank_workload(args.config, rank)
     r = bench_decode(wl, args, rank, world, device)
     step_bytes = decode_algorithmic_bytes(wl) + write_algorithmic_bytes(wl)
-    elapsed = torch.tensor([r["elapsed_ms"], r["e2e_ms"]], dtype=torch.float64, device=device)
-    units = torch.tensor([float(step_bytes), float(wl.num_seqs)], dtype=torch.float64,
-                         device=device)
-    if world > 1:
-        torch.distributed.all_reduce(elapsed, op=torch.distributed.ReduceOp.MAX)
-        torch.distributed.all_reduce(units, op=torch.distributed.ReduceOp.SUM)
+    (t_ms, e2e_ms), (total_bytes, total_seqs) = combine_ranks(
+        [r["elapsed_ms"], r["e2e_ms"]], [float(step_bytes), float(wl.num_seqs)], world, device)
     if rank != 0:
         torch.distributed.destroy_process_group()
         return
-    t_ms, e2e_ms = float(elapsed[0]), float(elapsed[1])
-    total_bytes, total_seqs = float(units[0]), float(units[1])
     per_step_ms = t_ms / args.steps
     value = total_bytes * args.steps / (t_ms / 1e3) / 1e9
     e2e_val = total_bytes * args.steps / (e2e_ms / 1e3) / 1e9
