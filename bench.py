@@ -289,6 +289,117 @@ def bench_decode(wl, args, rank, world, device):
     }
 
 
+def bench_prefill(wl, args, device):
+    """Chunked prefill step: paged write of the chunk's K/V + causal prefill."""
+    import paged_kv_cache_198_gb300 as tvl
+
+    base = W.to_device(wl, device)
+    cache_bytes = 2 * base["k_cache"].numel() * 2
+    copies = min(4, max(1, math.ceil(3 * L2_BYTES / max(1, cache_bytes)) + 1))
+    sets = [base] + [{k: (v.clone() if k in ("k_cache", "v_cache", "q") else v)
+                      for k, v in base.items()} for _ in range(copies - 1)]
+    out = torch.empty(tuple(wl.q.shape), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(t, ev=None):
+        tvl.paged_kv_write(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["slot_mapping"])
+        if ev is not None:
+            ev[0].record(stream)
+        tvl.paged_attention_prefill(out, t["q"], t["query_start_loc"], t["k_cache"],
+                                    t["v_cache"], t["block_tables"], t["context_lens"], wl.scale,
+                                    wl.max_q_len)
+        if ev is not None:
+            ev[1].record(stream)
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(device.index if device.index is not None else 0) as clocks:
+        time.sleep(0.5)
+        for i in range(args.warmup):
+            step(sets[i % copies])
+        torch.cuda.synchronize(device)
+        host_t0 = time.time()
+        start.record(stream)
+        for i in range(args.steps):
+            step(sets[i % copies], evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize(device)
+        host_t1 = time.time()
+        time.sleep(0.1)
+    if tvl.get_device_status() != 0:
+        raise RuntimeError("device status word set during timing")
+    host = {k: base[k].cpu().pin_memory() for k in ("q", "k_new", "v_new", "slot_mapping",
+                                                    "query_start_loc", "block_tables",
+                                                    "context_lens")}
+    out_host = torch.empty(tuple(wl.q.shape), dtype=torch.float32).pin_memory()
+    dev_in = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+
+    def e2e_step(t):
+        for k, v in host.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        tvl.paged_kv_write(dev_in["k_new"], dev_in["v_new"], t["k_cache"], t["v_cache"],
+                           dev_in["slot_mapping"])
+        tvl.paged_attention_prefill(out, dev_in["q"], dev_in["query_start_loc"], t["k_cache"],
+                                    t["v_cache"], dev_in["block_tables"],
+                                    dev_in["context_lens"], wl.scale, wl.max_q_len)
+        out_host.copy_(out, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(sets[i % copies])
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    e2e_steps = max(1, min(args.steps, 200))
+    for i in range(e2e_steps):
+        e2e_step(sets[i % copies])
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    return {
+        "elapsed_ms": start.elapsed_time(stop),
+        "kernel_ms": statistics.mean(a.elapsed_time(b) for a, b in evs),
+        "kernel_ms_median": statistics.median(a.elapsed_time(b) for a, b in evs),
+        "e2e_ms_per_step": e0.elapsed_time(e1) / e2e_steps,
+        "h2d": sum(v.numel() * v.element_size() for v in host.values()),
+        "d2h": out_host.numel() * out_host.element_size(), "copies": copies,
+        "clocks": clocks.summary(host_t0, host_t1),
+    }
+
+
+def prefill_line(wl, args, r, bf16_sus, peak_src):
+    flops = prefill_flops(wl)
+    per_step_ms = r["elapsed_ms"] / args.steps
+    achieved = flops / (r["kernel_ms"] / 1e3) / 1e12
+    return {
+        "metric": "chunked causal prefill TFLOP/s (causal-visible pairs, % of bf16 tensor peak)",
+        "value": round(flops / (per_step_ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(per_step_ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "num_seqs": wl.num_seqs,
+                   "heads": f"{wl.num_q_heads}/{wl.num_kv_heads}", "head_dim": wl.head_dim,
+                   "block_size": wl.block_size, "query_tokens": wl.total_q,
+                   "context_tokens": int(wl.context_lens.sum()),
+                   "causal_pairs": wl.causal_pairs(), "flops_per_step": flops,
+                   "step": "paged KV write of the chunk + causal prefill",
+                   "l2": f"{r['copies']} rotating copies of q and the caches"},
+        "roofline": {"kernel": "prefill_kernel", "bound": "tensor", "achieved": round(achieved, 1),
+                     "peak": bf16_sus, "unit": "TFLOP/s", "frac": round(achieved / bf16_sus, 4),
+                     "traffic": None,
+                     "peak_source": f"{peak_src} bf16_tflops_sustained (the kernel runs in a "
+                                    f"seconds-long loop)",
+                     "launch_ms_mean": round(r["kernel_ms"], 5),
+                     "launch_ms_median": round(r["kernel_ms_median"], 5)},
+        "e2e": {"value": round(flops / (r["e2e_ms_per_step"] / 1e3) / 1e12, 2),
+                "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": 2 * args.steps,
+        "clocks": r["clocks"],
+    }
+
+
 def cpu_baseline_decode(wl, budget_s=10.0):
     """The oracle (write + decode of the whole batch) on the host cores,
     repeated until about budget_s seconds have passed."""
@@ -328,7 +439,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--config", default="llama1b_decode",
-                    choices=["llama1b_decode", "continuous_batch", "long_splitk", "tiny"])
+                    choices=["llama1b_decode", "continuous_batch", "long_splitk", "tiny",
+                             "chunked_prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
@@ -392,6 +504,12 @@ def main():
         torch.distributed.barrier()
 
     wl = rank_workload(args.config, rank)
+    if args.config == "chunked_prefill":
+        if world > 1:
+            raise SystemExit("the prefill line is measured on one GPU")
+        print(json.dumps(prefill_line(wl, args, bench_prefill(wl, args, device), bf16_sus,
+                                      peak_src)))
+        return
     r = bench_decode(wl, args, rank, world, device)
     step_bytes = decode_algorithmic_bytes(wl) + write_algorithmic_bytes(wl)
     (t_ms, e2e_ms), (total_bytes, total_seqs) = combine_ranks(

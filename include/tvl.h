@@ -132,7 +132,7 @@ tvl_status tvl_paged_attention_decode_workspace_size(
  *   tvl_paged_attention_decode_workspace_size (may be NULL when that is 0);
  *   its contents on entry are ignored and on exit unspecified.
  * Supported: D == 64, G in {1, 2, 4, 8}, bs in {16, 32}, Hkv <= 8 or a
- * multiple of 8.
+ * multiple of 8 (for G == 8: Hkv <= 4 or a multiple of 4).
  */
 tvl_status tvl_paged_attention_decode(
     float* out, const void* q, const void* k_cache, const void* v_cache,

@@ -82,9 +82,11 @@ tvl_status check_heads(int hq, int hkv, int d) {
   return TVL_OK;
 }
 
-// Balanced decode: CTAs per KV-head group (one CTA per SM in total).
-int balanced_ctas(int sms, int hkv) {
-  const int hpc = hkv < 8 ? hkv : 8;
+// Balanced decode: CTAs per KV-head group (one CTA per SM in total); a CTA
+// owns up to 8 KV heads (4 for GQA groups of 8).
+int balanced_ctas(int sms, int hq, int hkv) {
+  const int hmax = hq / hkv >= 8 ? 4 : 8;
+  const int hpc = hkv < hmax ? hkv : hmax;
   const int groups = hkv / hpc;
   const int c = sms / groups;
   return c < 1 ? 1 : c;
@@ -100,8 +102,10 @@ tvl_status decode_sizes(int num_seqs, int hq, int hkv, int d, int mb, int bs, in
                 bs);
   tvl_status st = check_heads(hq, hkv, d);
   if (st != TVL_OK) return st;
-  if (hkv > 8 && hkv % 8 != 0)
-    return fail(TVL_ERR_UNSUPPORTED, "num_kv_heads %d (decode: <= 8 or a multiple of 8)", hkv);
+  const int hmax = hq / hkv >= 8 ? 4 : 8;   // KV heads one CTA owns
+  if (hkv > hmax && hkv % hmax != 0)
+    return fail(TVL_ERR_UNSUPPORTED, "num_kv_heads %d (decode: <= %d or a multiple of %d)", hkv,
+                hmax, hmax);
   *part_blocks = part / bs;
   *max_splits = part > 0 ? (mb + *part_blocks - 1) / *part_blocks : 0;
   *ctas = 0;
@@ -109,7 +113,7 @@ tvl_status decode_sizes(int num_seqs, int hq, int hkv, int d, int mb, int bs, in
     int sms = 0;
     st = sm_count(&sms);
     if (st != TVL_OK) return st;
-    *ctas = balanced_ctas(sms, hkv);
+    *ctas = balanced_ctas(sms, hq, hkv);
   } else if (num_seqs > 65535) {
     return fail(TVL_ERR_UNSUPPORTED, "num_seqs %d > 65535 with a fixed partition", num_seqs);
   }

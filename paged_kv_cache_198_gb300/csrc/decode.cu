@@ -20,21 +20,29 @@
 // writes a partial (m, l, acc) record, and merge_kernel combines the records
 // of a sequence by log-sum-exp -- the associative form of the online softmax.
 //
-// CTA structure.  One producer warp walks the CTA's segments and, per
-// physical block, issues 1-D bulk copies (TMA engine) of the block's K and V
-// for the CTA's KV heads (bs * Hkv * D * 2 contiguous bytes each when the CTA
-// owns every KV head) into a ring of shared-memory stages, with an mbarrier
-// per stage.  One consumer warp per KV head computes, per 16-token chunk:
+// CTA structure.  One producer warp walks the CTA's segments and, per stage
+// of 32 tokens (two physical blocks of 16 or one of 32), issues 1-D bulk
+// copies (TMA engine) of the blocks' K and V for the CTA's KV heads
+// (bs * Hkv * D * 2 contiguous bytes per block when the CTA owns every KV
+// head) into a ring of shared-memory stages, with an mbarrier per stage.
+// One consumer warp per KV head processes a stage as two 16-token chunks
+// whose instruction streams interleave:
 //   * q . k with lane = 8 * token_group + dim_chunk: each lane holds 8 dims
 //     of the G query heads (fp32, pre-scaled by scale * log2 e) and reads
-//     8 dims of 4 tokens (16-byte shared loads, conflict-free), packed
-//     fp32x2 FMAs; the 8-lane partial sums of the 4G (head, token) pairs are
-//     reduced with a transposing butterfly (4G/8 values per lane remain;
-//     the register order is permuted per lane so no selects are needed);
-//   * an online softmax in the exp2 domain whose running maximum is only
-//     moved when a score exceeds it by more than 2^8 (exact: the same
-//     reference maximum scales numerator and denominator);
-//   * p . V with p staged through a per-warp shared buffer, fp32x2 FMAs.
+//     8 dims of 4 tokens per chunk (16-byte shared loads, conflict-free),
+//     packed fp32x2 FMAs; the 8-lane partial sums of the 4G (head, token)
+//     pairs are reduced with a transposing butterfly (4G/8 values per lane
+//     remain; the register order is permuted per lane so no selects are
+//     needed);
+//   * an online softmax in the exp2 domain, one maximum per 32 tokens, whose
+//     running maximum is only moved when a score exceeds it by more than 2^8
+//     (exact: the same reference maximum scales numerator and denominator);
+//   * p . V with p staged through a per-warp shared buffer as duplicated
+//     pairs (p, p), so each fp32x2 FMA takes its operands straight from a
+//     16-byte shared load.
+// Launch: the kernels use programmatic dependent launch; each waits for its
+// predecessor's memory (griddepcontrol.wait) before touching any input, so
+// the next kernel's launch and prologue overlap the previous one's tail.
 // All waits are bounded; a timeout sets a status bit and the CTA leaves
 // after its copies in flight have landed.
 #include <cuda_bf16.h>
@@ -48,7 +56,12 @@ namespace {
 constexpr int kD = 64;
 constexpr uint32_t kRowBytes = kD * 2;   // one head's K or V row of one token
 constexpr int kChunk = 16;
+constexpr int kStageTokens = 32;
 constexpr int kMaxHeadsPerCta = 8;
+// KV heads (consumer warps) per CTA: with 9 warps, three share one
+// scheduler's register file (<= 168 registers a thread), too few for the
+// 8-head groups' q and accumulators; those CTAs take 4 KV heads.
+__host__ __device__ constexpr int max_heads_per_cta(int g) { return g >= 8 ? 4 : kMaxHeadsPerCta; }
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
@@ -86,6 +99,11 @@ struct Layout {
   uint32_t barriers, meta, pbuf, sched, total;
 };
 
+// Per-warp p buffer: 2 (double buffer) x 2 chunks x 4 token groups x 4G
+// (head, token) entries x 2 (duplicated pair).
+__host__ __device__ constexpr int kPbufFloats(int g) { return 2 * 2 * 4 * 4 * g * 2; }
+
+
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 __host__ __device__ inline Layout make_layout(int stages, uint32_t stage_bytes, int hpc, int g) {
@@ -96,7 +114,7 @@ __host__ __device__ inline Layout make_layout(int stages, uint32_t stage_bytes, 
   l.meta = align_up(off, 16);
   off = l.meta + stages * sizeof(StageMeta);
   l.pbuf = align_up(off, 16);
-  off = l.pbuf + hpc * 2 * 16 * g * 4;
+  off = l.pbuf + hpc * kPbufFloats(g) * 4;
   l.sched = align_up(off, 16);
   off = l.sched + 64 * 8;
   l.total = off;
@@ -172,7 +190,9 @@ __device__ void producer(const Params& p, const Schedule& sc, uint8_t* smem, con
   const int hg = blockIdx.z;
   const int hpc = p.hpc;
   const bool whole_rows = (hpc == p.hkv);
-  const uint32_t kv_bytes = BS * hpc * kRowBytes;
+  constexpr int BPS = kStageTokens / BS;               // physical blocks per stage
+  const uint32_t blk_bytes = BS * hpc * kRowBytes;     // one block, the CTA's heads
+  const uint32_t kv_bytes = kStageTokens * hpc * kRowBytes;
   const uint32_t q_bytes = hpc * G * kRowBytes;
   const uint64_t stream_policy = policy_evict_first();
   const uint64_t keep_policy = policy_evict_last();
@@ -217,20 +237,26 @@ __device__ void producer(const Params& p, const Schedule& sc, uint8_t* smem, con
     }
     const int32_t* table = p.block_tables + static_cast<long long>(s) * p.max_blocks;
     int tbl = 0;
-    for (long long blk = b; blk < e && ok; ++blk) {
-      const int slot = static_cast<int>((blk - b) & 31);
+    for (long long blk = b; blk < e && ok; blk += BPS) {
+      const int slot = static_cast<int>((blk - b) & 31);   // BPS divides 32
       if (slot == 0) tbl = (blk + lane < e) ? table[blk + lane] : 0;
-      int phys = __shfl_sync(kFull, tbl, slot);
-      if (phys < 0 || phys >= p.num_blocks) {
-        if (lane == 0) report(p.status, TVL_DEV_BAD_BLOCK_ID);
-        phys = 0;
+      const int nstage = (e - blk < BPS) ? static_cast<int>(e - blk) : BPS;
+      int phys[BPS];
+#pragma unroll
+      for (int i = 0; i < BPS; ++i) {
+        phys[i] = __shfl_sync(kFull, tbl, slot + i);
+        if (i < nstage && (phys[i] < 0 || phys[i] >= p.num_blocks)) {
+          if (lane == 0) report(p.status, TVL_DEV_BAD_BLOCK_ID);
+          phys[i] = 0;
+        }
       }
       int st;
       if (!acquire(st)) {
         ok = false;
         break;
       }
-      const int flags = (blk == b ? kSegFirst : 0) | (blk == e - 1 ? kSegLast : 0);
+      const bool first = (blk == b);
+      const int flags = (first ? kSegFirst : 0) | (blk + nstage >= e ? kSegLast : 0);
       uint8_t* kdst = smem + static_cast<size_t>(st) * p.stage_bytes;
       uint8_t* vdst = kdst + kv_bytes;
       uint8_t* qdst = vdst + kv_bytes;
@@ -238,30 +264,41 @@ __device__ void producer(const Params& p, const Schedule& sc, uint8_t* smem, con
         StageMeta m;
         m.seq = s;
         const long long rem = ctx - blk * BS;
-        m.valid = static_cast<int>(rem < BS ? rem : BS);
+        const long long cap = static_cast<long long>(nstage) * BS;
+        m.valid = static_cast<int>(rem < cap ? rem : cap);
         m.flags = flags;
         m.record = record;
         meta[st] = m;
-        mbar_arrive_expect_tx(&full[st], 2 * kv_bytes + ((flags & kSegFirst) ? q_bytes : 0));
+        mbar_arrive_expect_tx(&full[st], 2 * nstage * blk_bytes + (first ? q_bytes : 0));
       }
       __syncwarp();
-      const long long tok0 = static_cast<long long>(phys) * BS;
       if (whole_rows) {
-        if (lane == 0) {
-          const size_t off = static_cast<size_t>(tok0) * p.hkv * kD;
-          bulk_load(kdst, p.k_cache + off, kv_bytes, &full[st], stream_policy);
-          bulk_load(vdst, p.v_cache + off, kv_bytes, &full[st], stream_policy);
+        if (lane < nstage) {
+          int mine = phys[0];
+          if constexpr (BPS > 1) {
+            if (lane == 1) mine = phys[BPS - 1];
+          }
+          const size_t off = static_cast<size_t>(mine) * BS * p.hkv * kD;
+          bulk_load(kdst + lane * blk_bytes, p.k_cache + off, blk_bytes, &full[st],
+                    stream_policy);
+          bulk_load(vdst + lane * blk_bytes, p.v_cache + off, blk_bytes, &full[st],
+                    stream_policy);
         }
       } else {
-        for (int t = lane; t < BS; t += 32) {
-          const size_t off = (static_cast<size_t>(tok0 + t) * p.hkv + hg * hpc) * kD;
+        for (int t = lane; t < nstage * BS; t += 32) {
+          int mine = phys[0];
+          if constexpr (BPS > 1) {
+            if (t >= BS) mine = phys[BPS - 1];
+          }
+          const size_t off =
+              (static_cast<size_t>(mine) * BS * p.hkv + (t % BS) * p.hkv + hg * hpc) * kD;
           bulk_load(kdst + t * hpc * kRowBytes, p.k_cache + off, hpc * kRowBytes, &full[st],
                     stream_policy);
           bulk_load(vdst + t * hpc * kRowBytes, p.v_cache + off, hpc * kRowBytes, &full[st],
                     stream_policy);
         }
       }
-      if ((flags & kSegFirst) && lane == 1) {
+      if (first && lane == 31) {
         const size_t off = (static_cast<size_t>(s) * p.hq + hg * hpc * G) * kD;
         bulk_load(qdst, p.q + off, q_bytes, &full[st], keep_policy);
       }
@@ -349,61 +386,83 @@ struct ConsumerState {
   float l_part;       // this lane's share of the softmax denominator
 };
 
-template <int G, bool kFullChunk>
-__device__ __forceinline__ void process_chunk(ConsumerState<G>& st, const uint8_t* kbase,
-                                              const uint8_t* vbase, int row0, int valid,
-                                              int hpc, int w, float* pbuf) {
+// NCH 16-token chunks of a stage, starting at chunk chunk0 (tokens
+// [16 * chunk0, 16 * (chunk0 + NCH)) of the stage; `valid` counts tokens from
+// the stage start); kFull: every one of those tokens is inside the context.
+template <int G, int NCH, bool kFull>
+__device__ __forceinline__ void process_stage(ConsumerState<G>& st, const uint8_t* kbase,
+                                              const uint8_t* vbase, int valid, int hpc, int w,
+                                              float* pbuf, int chunk0 = 0) {
   using M = LaneMap<G>;
   const int lane = threadIdx.x & 31;
   const int c = lane & 7, tg = lane >> 3;
   const int mi = M::xor_mask(c) & 3;
   constexpr int N = 4 * G;
+  constexpr int R = M::kVals;
+  const int jb = M::jbase(c);
 
-  // --- scores: part[4*hr + ir] = q(head hr^mh) . k(token ir^mi) over 8 dims
-  float part[N];
+  // --- scores: part[ch][4*hr + ir] = q(head hr^mh) . k(token ir^mi) over 8 dims
+  float part[NCH][N];
 #pragma unroll
   for (int ir = 0; ir < 4; ++ir) {
-    const int t = row0 + tg * 4 + (ir ^ mi);
-    const uint4 kw =
-        *reinterpret_cast<const uint4*>(kbase + (t * hpc + w) * kRowBytes + c * 16);
-    const float2 k0 = bf16x2_to_float2(kw.x), k1 = bf16x2_to_float2(kw.y);
-    const float2 k2 = bf16x2_to_float2(kw.z), k3 = bf16x2_to_float2(kw.w);
 #pragma unroll
-    for (int hr = 0; hr < G; ++hr) {
-      float2 a = __fmul2_rn(st.qf[hr][0], k0);
-      a = __ffma2_rn(st.qf[hr][1], k1, a);
-      a = __ffma2_rn(st.qf[hr][2], k2, a);
-      a = __ffma2_rn(st.qf[hr][3], k3, a);
-      part[4 * hr + ir] = a.x + a.y;
+    for (int ch = 0; ch < NCH; ++ch) {
+      const int t = (chunk0 + ch) * kChunk + tg * 4 + (ir ^ mi);
+      const uint4 kw =
+          *reinterpret_cast<const uint4*>(kbase + (t * hpc + w) * kRowBytes + c * 16);
+      const float2 k0 = bf16x2_to_float2(kw.x), k1 = bf16x2_to_float2(kw.y);
+      const float2 k2 = bf16x2_to_float2(kw.z), k3 = bf16x2_to_float2(kw.w);
+#pragma unroll
+      for (int hr = 0; hr < G; ++hr) {
+        float2 a = __fmul2_rn(st.qf[hr][0], k0);
+        a = __ffma2_rn(st.qf[hr][1], k1, a);
+        a = __ffma2_rn(st.qf[hr][2], k2, a);
+        a = __ffma2_rn(st.qf[hr][3], k3, a);
+        part[ch][4 * hr + ir] = a.x + a.y;
+      }
     }
   }
   // --- transposing butterfly over the 8 dim-chunk lanes
   if constexpr (G >= 2) {
 #pragma unroll
-    for (int k = 0; k < N / 2; ++k) part[k] += __shfl_xor_sync(kFull, part[k + N / 2], 4);
+    for (int k = 0; k < N / 2; ++k)
 #pragma unroll
-    for (int k = 0; k < N / 4; ++k) part[k] += __shfl_xor_sync(kFull, part[k + N / 4], 2);
+      for (int ch = 0; ch < NCH; ++ch)
+        part[ch][k] += __shfl_xor_sync(kFull, part[ch][k + N / 2], 4);
 #pragma unroll
-    for (int k = 0; k < N / 8; ++k) part[k] += __shfl_xor_sync(kFull, part[k + N / 8], 1);
+    for (int k = 0; k < N / 4; ++k)
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch)
+        part[ch][k] += __shfl_xor_sync(kFull, part[ch][k + N / 4], 2);
+#pragma unroll
+    for (int k = 0; k < N / 8; ++k)
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch)
+        part[ch][k] += __shfl_xor_sync(kFull, part[ch][k + N / 8], 1);
   } else {
-    part[0] += __shfl_xor_sync(kFull, part[2], 4);
-    part[1] += __shfl_xor_sync(kFull, part[3], 4);
-    part[0] += __shfl_xor_sync(kFull, part[1], 2);
-    part[0] += __shfl_xor_sync(kFull, part[0], 1);
-  }
-  constexpr int R = M::kVals;
-  const int jb = M::jbase(c);
-  if constexpr (!kFullChunk) {
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int t = row0 + tg * 4 + ((jb + r) & 3);
-      if (t >= valid) part[r] = -INFINITY;
+    for (int ch = 0; ch < NCH; ++ch) {
+      part[ch][0] += __shfl_xor_sync(kFull, part[ch][2], 4);
+      part[ch][1] += __shfl_xor_sync(kFull, part[ch][3], 4);
+      part[ch][0] += __shfl_xor_sync(kFull, part[ch][1], 2);
+      part[ch][0] += __shfl_xor_sync(kFull, part[ch][0], 1);
     }
   }
-  // --- online softmax (exp2 domain, lazily moved reference maximum)
-  float cm = part[0];
+  if constexpr (!kFull) {
 #pragma unroll
-  for (int r = 1; r < R; ++r) cm = fmaxf(cm, part[r]);
+    for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int t = (chunk0 + ch) * kChunk + tg * 4 + ((jb + r) & 3);
+        if (t >= valid) part[ch][r] = -INFINITY;
+      }
+  }
+  // --- online softmax (exp2 domain, lazily moved reference maximum)
+  float cm = part[0][0];
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+    for (int r = 0; r < R; ++r) cm = fmaxf(cm, part[ch][r]);
   cm = reduce_max_head<G>(cm);
   if (__any_sync(kFull, cm > st.m_used + kRescaleLog2)) {
     const float m_new = fmaxf(st.m_used, cm);
@@ -418,42 +477,57 @@ __device__ __forceinline__ void process_chunk(ConsumerState<G>& st, const uint8_
       for (int k = 0; k < 4; ++k) st.acc[h][k] = __fmul2_rn(st.acc[h][k], ff);
     }
   }
-  float pr[R];
+  // p as duplicated pairs: pbuf[ch][tg][j = 4*head + token][2]
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    pr[r] = ex2(part[r] - st.m_used);
-    if (G > 1 || (c & 1) == 0) st.l_part += pr[r];
-  }
-  float* pb = pbuf + tg * N;
-  if constexpr (R == 4) {
-    *reinterpret_cast<float4*>(pb + jb) = make_float4(pr[0], pr[1], pr[2], pr[3]);
-  } else if constexpr (R == 2) {
-    *reinterpret_cast<float2*>(pb + jb) = make_float2(pr[0], pr[1]);
-  } else {
-    pb[jb] = pr[0];
+  for (int ch = 0; ch < NCH; ++ch) {
+    float pr[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      pr[r] = ex2(part[ch][r] - st.m_used);
+      if (G > 1 || (c & 1) == 0) st.l_part += pr[r];
+    }
+    float* pb = pbuf + ((chunk0 + ch) * 4 + tg) * N * 2 + jb * 2;
+    if constexpr (R == 4) {
+      reinterpret_cast<float4*>(pb)[0] = make_float4(pr[0], pr[0], pr[1], pr[1]);
+      reinterpret_cast<float4*>(pb)[1] = make_float4(pr[2], pr[2], pr[3], pr[3]);
+    } else if constexpr (R == 2) {
+      *reinterpret_cast<float4*>(pb) = make_float4(pr[0], pr[0], pr[1], pr[1]);
+    } else {
+      *reinterpret_cast<float2*>(pb) = make_float2(pr[0], pr[0]);
+    }
   }
   __syncwarp();
   // --- o += p . V
-  float4 ph[G];
 #pragma unroll
-  for (int h = 0; h < G; ++h) ph[h] = *reinterpret_cast<const float4*>(pb + 4 * h);
+  for (int ch = 0; ch < NCH; ++ch) {
+    const float* pb = pbuf + ((chunk0 + ch) * 4 + tg) * N * 2;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = row0 + tg * 4 + i;
-    uint4 vw = *reinterpret_cast<const uint4*>(vbase + (t * hpc + w) * kRowBytes + c * 16);
-    if constexpr (!kFullChunk) {
-      if (t >= valid) vw = make_uint4(0, 0, 0, 0);   // unused slots may hold anything
-    }
-    const float2 v0 = bf16x2_to_float2(vw.x), v1 = bf16x2_to_float2(vw.y);
-    const float2 v2 = bf16x2_to_float2(vw.z), v3 = bf16x2_to_float2(vw.w);
+    for (int i = 0; i < 4; i += 2) {
+      const int t0 = (chunk0 + ch) * kChunk + tg * 4 + i;
+      uint4 vw0 = *reinterpret_cast<const uint4*>(vbase + (t0 * hpc + w) * kRowBytes + c * 16);
+      uint4 vw1 =
+          *reinterpret_cast<const uint4*>(vbase + ((t0 + 1) * hpc + w) * kRowBytes + c * 16);
+      if constexpr (!kFull) {   // slots past the context may hold anything
+        if (t0 >= valid) vw0 = make_uint4(0, 0, 0, 0);
+        if (t0 + 1 >= valid) vw1 = make_uint4(0, 0, 0, 0);
+      }
+      const float2 a0 = bf16x2_to_float2(vw0.x), a1 = bf16x2_to_float2(vw0.y);
+      const float2 a2 = bf16x2_to_float2(vw0.z), a3 = bf16x2_to_float2(vw0.w);
+      const float2 b0 = bf16x2_to_float2(vw1.x), b1 = bf16x2_to_float2(vw1.y);
+      const float2 b2 = bf16x2_to_float2(vw1.z), b3 = bf16x2_to_float2(vw1.w);
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float pv = i == 0 ? ph[h].x : i == 1 ? ph[h].y : i == 2 ? ph[h].z : ph[h].w;
-      const float2 pp = make_float2(pv, pv);
-      st.acc[h][0] = __ffma2_rn(pp, v0, st.acc[h][0]);
-      st.acc[h][1] = __ffma2_rn(pp, v1, st.acc[h][1]);
-      st.acc[h][2] = __ffma2_rn(pp, v2, st.acc[h][2]);
-      st.acc[h][3] = __ffma2_rn(pp, v3, st.acc[h][3]);
+      for (int h = 0; h < G; ++h) {
+        const float4 pp = *reinterpret_cast<const float4*>(pb + (4 * h + i) * 2);
+        const float2 p0 = make_float2(pp.x, pp.y), p1 = make_float2(pp.z, pp.w);
+        st.acc[h][0] = __ffma2_rn(p0, a0, st.acc[h][0]);
+        st.acc[h][1] = __ffma2_rn(p0, a1, st.acc[h][1]);
+        st.acc[h][2] = __ffma2_rn(p0, a2, st.acc[h][2]);
+        st.acc[h][3] = __ffma2_rn(p0, a3, st.acc[h][3]);
+        st.acc[h][0] = __ffma2_rn(p1, b0, st.acc[h][0]);
+        st.acc[h][1] = __ffma2_rn(p1, b1, st.acc[h][1]);
+        st.acc[h][2] = __ffma2_rn(p1, b2, st.acc[h][2]);
+        st.acc[h][3] = __ffma2_rn(p1, b3, st.acc[h][3]);
+      }
     }
   }
 }
@@ -517,8 +591,8 @@ __device__ void consumer(const Params& p, uint8_t* smem, const Layout& L) {
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.barriers);
   uint64_t* empty = full + p.stages;
   const StageMeta* meta = reinterpret_cast<const StageMeta*>(smem + L.meta);
-  float* pbuf_w = reinterpret_cast<float*>(smem + L.pbuf) + w * 2 * 16 * G;
-  const uint32_t kv_bytes = BS * hpc * kRowBytes;
+  float* pbuf_w = reinterpret_cast<float*>(smem + L.pbuf) + w * kPbufFloats(G);
+  const uint32_t kv_bytes = kStageTokens * hpc * kRowBytes;
 
   ConsumerState<G> st;
   st.m_used = -INFINITY;
@@ -530,7 +604,7 @@ __device__ void consumer(const Params& p, uint8_t* smem, const Layout& L) {
       st.acc[h][k] = make_float2(0.f, 0.f);
       st.qf[h][k] = make_float2(0.f, 0.f);
     }
-  int chunk_no = 0;
+  int stage_no = 0;
   for (long long it = 0;; ++it) {
     const int s = static_cast<int>(it % p.stages);
     if (!mbar_wait(&full[s], static_cast<uint32_t>((it / p.stages) & 1))) {
@@ -558,18 +632,27 @@ __device__ void consumer(const Params& p, uint8_t* smem, const Layout& L) {
         for (int k = 0; k < 4; ++k) st.acc[hr][k] = make_float2(0.f, 0.f);
       }
     }
-#pragma unroll
-    for (int ch = 0; ch < BS / kChunk; ++ch) {
-      const int row0 = ch * kChunk;
-      if (row0 < md.valid) {
-        float* pb = pbuf_w + (chunk_no & 1) * 16 * G;
-        if (md.valid >= row0 + kChunk)
-          process_chunk<G, true>(st, kbase, vbase, row0, md.valid, hpc, w, pb);
+    float* pb = pbuf_w + (stage_no & 1) * (kPbufFloats(G) / 2);
+    if (md.valid > kChunk) {
+      if constexpr (G <= 4) {     // both chunks at once: twice the independent work
+        if (md.valid >= kStageTokens)
+          process_stage<G, 2, true>(st, kbase, vbase, md.valid, hpc, w, pb);
         else
-          process_chunk<G, false>(st, kbase, vbase, row0, md.valid, hpc, w, pb);
-        ++chunk_no;
+          process_stage<G, 2, false>(st, kbase, vbase, md.valid, hpc, w, pb);
+      } else {                    // G = 8 would run out of registers: one at a time
+        process_stage<G, 1, true>(st, kbase, vbase, md.valid, hpc, w, pb, 0);
+        if (md.valid >= kStageTokens)
+          process_stage<G, 1, true>(st, kbase, vbase, md.valid, hpc, w, pb, 1);
+        else
+          process_stage<G, 1, false>(st, kbase, vbase, md.valid, hpc, w, pb, 1);
       }
+    } else {
+      if (md.valid >= kChunk)
+        process_stage<G, 1, true>(st, kbase, vbase, md.valid, hpc, w, pb);
+      else
+        process_stage<G, 1, false>(st, kbase, vbase, md.valid, hpc, w, pb);
     }
+    ++stage_no;
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
     if (md.flags & kSegLast) finish_segment<G>(st, p, md.seq, md.record, hq0);
@@ -579,7 +662,8 @@ __device__ void consumer(const Params& p, uint8_t* smem, const Layout& L) {
 // ------------------------------------------------------------------ kernel
 
 template <int G, int BS>
-__global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32, 1) decode_kernel(const Params p) {
+__global__ void __launch_bounds__((max_heads_per_cta(G) + 1) * 32, 1)
+    decode_kernel(const Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const Layout L = make_layout(p.stages, p.stage_bytes, p.hpc, G);
   Schedule* sched = reinterpret_cast<Schedule*>(smem + L.sched);
@@ -595,6 +679,8 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32, 1) decode_kernel(c
     }
     fence_barrier_init();
   }
+  grid_dependency_wait();        // inputs may come from the preceding kernel
+  grid_dependents_launch();
 
   if (p.partition_blocks > 0) {
     // fixed windows: CTA (x = window, y = sequence)
@@ -698,6 +784,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
     count = (nb + p.partition_blocks - 1) / p.partition_blocks;
   } else {
     if (nb == 0) {
+      grid_dependency_wait();
       if (h < p.hq) {
         float* dst = p.out + (static_cast<long long>(s) * p.hq + h) * kD;
         dst[lane] = 0.f;
@@ -721,6 +808,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
     c_last = balanced_cta_of(seq_start + nb - 1, total, C);
     if (c_first == c_last) return;   // one CTA held the whole sequence
   }
+  grid_dependency_wait();        // the decode's records must be complete
   if (h >= p.hq) return;
 
   // record index of the k-th candidate, or -1 when that CTA holds none of s
@@ -765,8 +853,7 @@ cudaError_t launch_t(const Params& prm, dim3 grid, uint32_t smem_bytes, cudaStre
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
-  kern<<<grid, (prm.hpc + 1) * 32, smem_bytes, stream>>>(prm);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3((prm.hpc + 1) * 32), smem_bytes, stream, prm);
 }
 
 }  // namespace
@@ -804,7 +891,8 @@ DecodeWorkspace decode_workspace_carve(void* base, long long records, int num_q_
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (a.num_seqs == 0) return cudaSuccess;
   const int G = a.num_q_heads / a.num_kv_heads;
-  const int hpc = a.num_kv_heads < kMaxHeadsPerCta ? a.num_kv_heads : kMaxHeadsPerCta;
+  const int hmax = max_heads_per_cta(G);
+  const int hpc = a.num_kv_heads < hmax ? a.num_kv_heads : hmax;
   const int groups = a.num_kv_heads / hpc;
   const int bs = a.block_size;
 
@@ -821,7 +909,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   prm.num_blocks = a.num_blocks;
   prm.max_blocks = a.max_blocks_per_seq;
   prm.hpc = hpc;
-  prm.stage_bytes = align_up(2 * bs * hpc * kRowBytes + hpc * G * kRowBytes, 128);
+  prm.stage_bytes = align_up(2 * kStageTokens * hpc * kRowBytes + hpc * G * kRowBytes, 128);
   const uint32_t fixed_part = make_layout(0, prm.stage_bytes, hpc, G).total + 2 * 8 * 8 + 16 * 8;
   int stages = static_cast<int>((kSmemBudget - fixed_part) / prm.stage_bytes);
   stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
@@ -871,8 +959,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   mp.ws = a.ws;
   mp.status = a.status;
   dim3 mgrid(a.num_seqs, (a.num_q_heads + kMergeWarps - 1) / kMergeWarps);
-  merge_kernel<<<mgrid, kMergeWarps * 32, 0, stream>>>(mp);
-  return cudaGetLastError();
+  return launch_pdl(merge_kernel, mgrid, dim3(kMergeWarps * 32), 0, stream, mp);
 }
 
 }  // namespace tvl

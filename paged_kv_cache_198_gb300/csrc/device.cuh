@@ -4,7 +4,9 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_bf16.h>
+#include <cuda_runtime.h>
 
 #include "../../include/tvl.h"
 
@@ -106,6 +108,37 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 // to two floats; exact.
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// ------------------------------------------------- programmatic launch
+
+// Waits until the preceding kernel in the stream has completed and its
+// memory is visible (a no-op when the kernel was launched normally).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel in the stream start its launch and prologue.
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launches `kern` with programmatic stream serialization: it may start while
+// its predecessor finishes, and must call grid_dependency_wait() before it
+// reads anything the predecessor may write.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 }  // namespace tvl

@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
                     uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
                     const int32_t* __restrict__ slot_mapping, int num_tokens, int row_vecs,
                     long long num_slots, uint32_t* status) {
+  grid_dependency_wait();        // inputs may come from the preceding kernel
+  grid_dependents_launch();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const long long t = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + warp;
@@ -49,11 +51,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 cudaError_t launch_kv_write(const KvWriteArgs& a, cudaStream_t stream) {
   if (a.num_tokens == 0) return cudaSuccess;
   const int blocks = (a.num_tokens + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  kv_write_kernel<<<blocks, kWarpsPerBlock * 32, 0, stream>>>(
-      static_cast<const uint4*>(a.k_new), static_cast<const uint4*>(a.v_new),
-      static_cast<uint4*>(a.k_cache), static_cast<uint4*>(a.v_cache), a.slot_mapping,
-      a.num_tokens, a.row_bytes / 16, a.num_slots, a.status);
-  return cudaGetLastError();
+  return launch_pdl(kv_write_kernel, dim3(blocks), dim3(kWarpsPerBlock * 32), 0, stream,
+                    static_cast<const uint4*>(a.k_new), static_cast<const uint4*>(a.v_new),
+                    static_cast<uint4*>(a.k_cache), static_cast<uint4*>(a.v_cache),
+                    a.slot_mapping, a.num_tokens, a.row_bytes / 16, a.num_slots, a.status);
 }
 
 }  // namespace tvl

@@ -254,6 +254,21 @@ def named(name: str, replica: int = 0):
     raise KeyError(name)
 
 
+def share_prefix(wl, prefix_blocks: int) -> None:
+    """Prefix caching [nano-vLLM guide ch. 7]: make every sequence's first
+    `prefix_blocks` logical blocks the same physical blocks as sequence 0's
+    (in place).  Sequences must all have more than prefix_blocks blocks.  The
+    blocks a sequence gave up stay in the pool, unused."""
+    bs = wl.block_size
+    nb = [(int(c) + bs - 1) // bs for c in wl.context_lens.tolist()]
+    if min(nb) <= prefix_blocks:
+        raise ValueError("every sequence must extend past the shared prefix")
+    wl.block_tables[1:, :prefix_blocks] = wl.block_tables[0, :prefix_blocks]
+    if hasattr(wl, "slot_mapping") and wl.slot_mapping.numel():
+        # the new tokens live past the prefix, in private blocks: slots unchanged
+        pass
+
+
 def poison_unused(wl, value: float = 1.0e4) -> None:
     """Fill every cache slot that no sequence reads (whole unused blocks and
     the tail of each sequence's last block) with a large finite value, in
