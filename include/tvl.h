@@ -167,6 +167,29 @@ tvl_status tvl_paged_attention_prefill(
     int block_size, int num_blocks, int max_blocks_per_seq, float scale,
     void* stream);
 
+/*
+ * Decode without a caller workspace.  No counterpart on the source pages: it
+ * exists for callers that cannot allocate device memory where they decode --
+ * an engine that gave all device memory to its KV pool up front, a plugin or
+ * callback interface that hands over only input and output pointers, or a
+ * thread that must not block on the driver's allocation lock.
+ * Same arguments, layouts and results as tvl_paged_attention_decode, minus
+ * the workspace: the split-K partial records go to one built-in device array
+ * of 4 MiB (held by every GPU that loads the library until exit).  A call
+ * that needs more scratch than that returns TVL_ERR_WORKSPACE and launches
+ * nothing.  The call allocates and frees nothing.
+ * Set-up: the first call on a device (with that device current) looks up the
+ * array's device address once; make that first call before any stream
+ * capture.  Calls share the array: nothing needs clearing between calls, but
+ * calls that overlap on the GPU race on it.
+ */
+tvl_status tvl_paged_attention_decode_noalloc(
+    float* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+    int num_blocks, int max_blocks_per_seq, float scale, int partition_size,
+    void* stream);
+
 /* Static description of a status code. */
 const char* tvl_status_string(tvl_status status);
 

@@ -125,6 +125,10 @@ tvl_status decode_sizes(int num_seqs, int hq, int hkv, int d, int mb, int bs, in
 
 }  // namespace
 
+namespace tvl {
+void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+}  // namespace tvl
+
 extern "C" {
 
 const char* tvl_status_string(tvl_status status) {

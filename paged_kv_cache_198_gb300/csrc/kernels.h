@@ -72,4 +72,7 @@ struct PrefillArgs {
 };
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 
+// Sets the calling thread's tvl_last_error() text.
+void set_last_error(const char* msg);
+
 }  // namespace tvl
