@@ -758,7 +758,8 @@ struct MergeParams {
   uint32_t* status;
 };
 
-constexpr int kMergeWarps = 8;
+constexpr int kMergeWarps = 4;       // one warp per query head
+constexpr int kMergeMaxRecords = 512; // record indices staged per pass
 
 __device__ __forceinline__ int merge_ctx(const MergeParams& p, int s) {
   int c = p.context_lens[s];
@@ -768,20 +769,22 @@ __device__ __forceinline__ int merge_ctx(const MergeParams& p, int s) {
 
 // Combines the partial records of one sequence:
 //   M = max_r m_r;  out = sum_r 2^(m_r - M) acc_r / sum_r 2^(m_r - M) l_r.
+// Small (128 threads, few registers) so that its CTAs fit beside the decode
+// CTAs and run their prologue -- the record list, which depends only on the
+// context lengths -- while the decode finishes.
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeParams p) {
   __shared__ long long tmp[32];
+  __shared__ int recs[kMergeMaxRecords];
   const int s = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int h = blockIdx.y * kMergeWarps + warp;
   const long long nb = (merge_ctx(p, s) + p.bs - 1) / p.bs;
-
-  long long first = 0, count = 0;    // fixed mode record list
-  long long seq_start = 0, total = 0, c_first = 0, c_last = -1;
   const bool fixed = p.partition_blocks > 0;
+
+  long long n_cand = 0, seq_start = 0, total = 0, c_first = 0;
   if (fixed) {
     if (nb <= p.partition_blocks) return;   // single window: decode wrote the output
-    first = static_cast<long long>(s) * p.max_splits;
-    count = (nb + p.partition_blocks - 1) / p.partition_blocks;
+    n_cand = (nb + p.partition_blocks - 1) / p.partition_blocks;
   } else {
     if (nb == 0) {
       grid_dependency_wait();
@@ -805,42 +808,62 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
     seq_start = all;
     const long long C = p.balanced_ctas;
     c_first = balanced_cta_of(seq_start, total, C);
-    c_last = balanced_cta_of(seq_start + nb - 1, total, C);
+    const long long c_last = balanced_cta_of(seq_start + nb - 1, total, C);
     if (c_first == c_last) return;   // one CTA held the whole sequence
+    n_cand = c_last - c_first + 1;
   }
-  grid_dependency_wait();        // the decode's records must be complete
-  if (h >= p.hq) return;
 
-  // record index of the k-th candidate, or -1 when that CTA holds none of s
-  auto record_of = [&](long long k) -> long long {
-    if (fixed) return first + k;
+  // record index of candidate k, or -1 when that CTA holds none of s
+  auto record_of = [&](long long k) -> int {
+    if (fixed) return static_cast<int>(static_cast<long long>(s) * p.max_splits + k);
     const long long c = c_first + k;
     const long long lo = total * c / p.balanced_ctas;
     const long long hi = total * (c + 1) / p.balanced_ctas;
     const long long a = lo > seq_start ? lo : seq_start;
     const long long b = hi < seq_start + nb ? hi : seq_start + nb;
     if (a >= b) return -1;
-    return 2 * c + (seq_start <= lo ? 0 : 1);
+    return static_cast<int>(2 * c + (seq_start <= lo ? 0 : 1));
   };
-  const long long n_cand = fixed ? count : (c_last - c_first + 1);
 
-  float mx = -INFINITY;
-  for (long long k = lane; k < n_cand; k += 32) {
-    const long long r = record_of(k);
-    if (r >= 0) mx = fmaxf(mx, p.ws.m[r * p.hq + h]);
-  }
+  float mx = -INFINITY, den = 0.f, o0 = 0.f, o1 = 0.f;
+  bool waited = false;
+  for (long long base = 0; base < n_cand; base += kMergeMaxRecords) {
+    const int n = static_cast<int>(n_cand - base < kMergeMaxRecords ? n_cand - base
+                                                                     : kMergeMaxRecords);
+    if (base > 0) __syncthreads();
+    for (int k = tid; k < n; k += blockDim.x) recs[k] = record_of(base + k);
+    __syncthreads();
+    if (!waited) {
+      grid_dependency_wait();      // the decode's records must be complete
+      waited = true;
+    }
+    if (h >= p.hq) continue;
+    // running maximum over this pass's records (lanes split the records)
+    float pm = -INFINITY;
+    for (int k = lane; k < n; k += 32) {
+      const int r = recs[k];
+      if (r >= 0) pm = fmaxf(pm, p.ws.m[static_cast<long long>(r) * p.hq + h]);
+    }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-  float den = 0.f, o0 = 0.f, o1 = 0.f;
-  for (long long k = 0; k < n_cand; ++k) {
-    const long long r = record_of(k);
-    if (r < 0) continue;
-    const long long row = r * p.hq + h;
-    const float wgt = ex2(p.ws.m[row] - mx);
-    den += wgt * p.ws.l[row];
-    o0 += wgt * p.ws.acc[row * kD + lane];
-    o1 += wgt * p.ws.acc[row * kD + lane + 32];
+    for (int o = 16; o > 0; o >>= 1) pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, o));
+    const float m_new = fmaxf(mx, pm);
+    const float f = ex2(mx - m_new);     // 0 on the first pass
+    den *= f;
+    o0 *= f;
+    o1 *= f;
+    mx = m_new;
+#pragma unroll 4
+    for (int k = 0; k < n; ++k) {
+      const int r = recs[k];
+      if (r < 0) continue;
+      const long long row = static_cast<long long>(r) * p.hq + h;
+      const float wgt = ex2(p.ws.m[row] - mx);
+      den += wgt * p.ws.l[row];
+      o0 += wgt * p.ws.acc[row * kD + lane];
+      o1 += wgt * p.ws.acc[row * kD + lane + 32];
+    }
   }
+  if (h >= p.hq) return;
   const float inv = 1.0f / den;
   float* dst = p.out + (static_cast<long long>(s) * p.hq + h) * kD;
   dst[lane] = o0 * inv;
