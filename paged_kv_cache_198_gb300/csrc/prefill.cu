@@ -8,26 +8,32 @@
 // the Lq new query tokens of a sequence are its last Lq positions; row i at
 // absolute position p = ctx - Lq + i attends to cached tokens 0..p.
 //
-// One CTA = one 128-row query tile of one query head.  Warps:
-//   0-3  softmax: thread r owns query row r (TMEM lane r); reads S from TMEM,
-//        masks, keeps the running maximum (moved lazily: only when a score
-//        exceeds it by more than 2^8, which keeps the result exact), writes
-//        P = 2^(S*scale*log2e - m) as fp16 into a 128-byte-swizzled K-major
-//        shared tile, converts the V tile bf16 -> fp16 in place (exact for
-//        |v| >= 2^-14), rescales O in TMEM when the maximum moved, and finally
-//        normalises O and stores it;
-//   4    producer: TMA loads of the Q tile and, per 128-key tile, one box of
-//        bs tokens x 64 dims per physical block (K and V) found through the
-//        block table -- the paged gather; blocks past the context are read
-//        out of range so TMA fills them with zeros;
-//   5    MMA issuer: S = Q K^T (M 128, N 128, bf16 inputs) into one of two
-//        TMEM buffers, then O += P V (M 128, N 64, fp16 inputs), fp32
-//        accumulation throughout; completion is signalled with
-//        tcgen05.commit on mbarriers.
+// One CTA = one 128-row query tile of NH query heads of the same GQA group
+// (NH = 2 when the group has two or more heads), so each K/V tile gathered
+// from the paged cache serves NH heads.  Warps:
+//   0..4NH-1  softmax, one warpgroup per head: thread r owns query row r
+//             (TMEM lane r).  Per 128-key tile it converts its share of the V
+//             tile bf16 -> fp16 in place (exact for |v| >= 2^-14; keys past
+//             the context become 0), finds the row maximum of S, keeps a
+//             running maximum that moves only when a score exceeds it by more
+//             than 2^8 (exact: one reference maximum scales numerator and
+//             denominator; O in TMEM is rescaled when it moves), computes
+//             P = 2^(S*scale*log2e - m) with packed fp32x2 arithmetic and
+//             stores it as fp16 into TMEM; at the end it normalises O and
+//             writes it out;
+//   4NH       producer: TMA loads of the Q tiles and, per 128-key tile, one
+//             box of bs tokens x 64 dims per physical block (K and V) found
+//             through the block table -- the paged gather; blocks past the
+//             context are requested out of range, so TMA fills them with 0;
+//   4NH+1     MMA issuer: S_h = Q_h K^T (M 128, N 128, bf16, both operands in
+//             shared memory) and O_h += P_h V (M 128, N 64, fp16, P read from
+//             TMEM, V an MN-major shared operand), fp32 accumulation; the
+//             heads' MMAs alternate so one head's softmax overlaps the other
+//             head's tensor work.  Completion is signalled by tcgen05.commit.
 // P and V go through fp16 rather than bf16 so that rounding P costs at most
 // 2^-11 relative (bf16 would cost 2^-8) -- the fp32-accumulated result stays
 // within 2e-3 of the exact attention even for rows with few keys.
-// TMEM: S0 [0,128), S1 [128,256), O [256,320) of a 512-column allocation.
+// TMEM (per head h): S_h 128 columns, O_h 64, P_h 64 (fp16 pairs).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -45,40 +51,45 @@ namespace {
 constexpr int kD = 64;
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-constexpr int kThreads = 192;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 256;
+constexpr int kStages = 3;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
-
 constexpr uint32_t kTileBytes = kBM * kD * 2;      // 16 KB: 128 rows x 128 B
-constexpr uint32_t kQOff = 0;
-constexpr uint32_t kKOff = kQOff + kTileBytes;      // 2 stages
-constexpr uint32_t kVOff = kKOff + 2 * kTileBytes;  // 2 stages
-constexpr uint32_t kPOff = kVOff + 2 * kTileBytes;  // 2 buffers of 2 x 16 KB
-constexpr uint32_t kBarOff = kPOff + 4 * kTileBytes;
-constexpr uint32_t kSmemUsed = kBarOff + 256;
-constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack to align the base to 1 KB
 
 constexpr uint32_t kIdescQK = idesc_f16_f32acc(1, 0, kBM, kBN);   // bf16, K-major B
 constexpr uint32_t kIdescPV = idesc_f16_f32acc(0, 1, kBM, kD);    // fp16, MN-major B
 
+template <int NH>
+struct Cfg {
+  static constexpr int kSoftmaxWarps = 4 * NH;
+  static constexpr int kProducerWarp = kSoftmaxWarps;
+  static constexpr int kMmaWarp = kSoftmaxWarps + 1;
+  static constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+  static constexpr uint32_t kQOff = 0;
+  static constexpr uint32_t kKOff = NH * kTileBytes;
+  static constexpr uint32_t kVOff = kKOff + kStages * kTileBytes;
+  static constexpr uint32_t kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr uint32_t kSmemBytes = kBarOff + 512 + 1024;   // + 1 KB alignment slack
+  static constexpr uint32_t kTmemCols = NH == 2 ? 512 : 256;
+  __device__ static uint32_t s_col(int h) { return h * kBN; }
+  __device__ static uint32_t o_col(int h) { return NH * kBN + h * kD; }
+  __device__ static uint32_t p_col(int h) { return NH * (kBN + kD) + h * (kBN / 2); }
+};
+
 struct Barriers {
   uint64_t q_full;
-  uint64_t kv_full[2];
-  uint64_t kv_empty[2];
+  uint64_t kv_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t v_ready[kStages];
   uint64_t s_full[2];
-  uint64_t s_free[2];
   uint64_t p_full[2];
   uint64_t pv_done[2];
   uint64_t mma_done;
   uint32_t tmem_base;
   uint32_t abort;
 };
-static_assert(sizeof(Barriers) <= 256, "barrier area");
+static_assert(sizeof(Barriers) <= 512, "barrier area");
 
 struct Params {
   float* out;
@@ -93,6 +104,18 @@ struct Params {
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
+__device__ __forceinline__ float min3(float a, float b, float c) {
+  float y;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
   return y;
 }
 
@@ -116,26 +139,31 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
   return false;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <int NH>
+__global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  using C = Cfg<NH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  Barriers* B = reinterpret_cast<Barriers*>(smem + kBarOff);
+  Barriers* B = reinterpret_cast<Barriers*>(smem + C::kBarOff);
 
   const int qtile = p.n_qtiles - 1 - static_cast<int>(blockIdx.x);   // longest tiles first
-  const int h = blockIdx.y;
+  const int h0 = blockIdx.y * NH;                                     // first query head
   const int s = blockIdx.z;
-  const int g = h / p.group;
+  const int g = h0 / p.group;                                         // shared KV head
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+
+  grid_dependency_wait();          // inputs may come from the preceding kernel
+  grid_dependents_launch();
 
   // ---- per-tile geometry (identical in every thread)
   const int q0 = p.query_start_loc[s];
   const int lq = p.query_start_loc[s + 1] - q0;
-  int ctx = p.context_lens[s];
+  const int ctx = p.context_lens[s];
   const int cap = p.max_blocks * p.bs;
   if (qtile * kBM >= lq) return;                       // no rows here
   if (ctx < lq || ctx > cap || lq < 0) {
@@ -154,11 +182,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&B->q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&B->kv_full[i], 1);
       mbar_init(&B->kv_empty[i], 1);
+      mbar_init(&B->v_ready[i], C::kSoftmaxWarps);
+    }
+    for (int i = 0; i < NH; ++i) {
       mbar_init(&B->s_full[i], 1);
-      mbar_init(&B->s_free[i], 4);
       mbar_init(&B->p_full[i], 4);
       mbar_init(&B->pv_done[i], 1);
     }
@@ -167,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   if (warp == 0) {
-    tmem_alloc(&B->tmem_base, kTmemCols);
+    tmem_alloc(&B->tmem_base, C::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -175,20 +205,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = B->tmem_base;
 
-  if (warp == kProducerWarp) {
+  if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);
-      mbar_arrive_expect_tx(&B->q_full, kTileBytes);
-      tma_load_3d(smem + kQOff, &tm_q, 0, h, q0 + row0, &B->q_full);
+      mbar_arrive_expect_tx(&B->q_full, NH * kTileBytes);
+      for (int i = 0; i < NH; ++i)
+        tma_load_3d(smem + C::kQOff + i * kTileBytes, &tm_q, 0, h0 + i, q0 + row0, &B->q_full);
     }
     const int32_t* table = p.block_tables + static_cast<long long>(s) * p.max_blocks;
     for (int j = 0; j < n_kv; ++j) {
-      const int st = j & 1;
+      const int st = j % kStages;
       bool ok = true;
-      if (j >= 2 && lane == 0) ok = wait_or_abort(&B->kv_empty[st], ((j - 2) >> 1) & 1, B, p);
+      if (j >= kStages && lane == 0)
+        ok = wait_or_abort(&B->kv_empty[st], ((j / kStages) - 1) & 1, B, p);
       if (__shfl_sync(kFull, ok ? 1 : 0, 0) == 0) break;
       if (lane == 0) mbar_arrive_expect_tx(&B->kv_full[st], 2 * kTileBytes);
       __syncwarp();
@@ -203,179 +235,229 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const uint32_t off = static_cast<uint32_t>(b * p.bs) * (kD * 2);
-        tma_load_4d(smem + kKOff + st * kTileBytes + off, &tm_k, 0, g, 0, phys, &B->kv_full[st]);
-        tma_load_4d(smem + kVOff + st * kTileBytes + off, &tm_v, 0, g, 0, phys, &B->kv_full[st]);
+        tma_load_4d(smem + C::kKOff + st * kTileBytes + off, &tm_k, 0, g, 0, phys,
+                    &B->kv_full[st]);
+        tma_load_4d(smem + C::kVOff + st * kTileBytes + off, &tm_v, 0, g, 0, phys,
+                    &B->kv_full[st]);
       }
     }
-    // the loads of the last (up to) two tiles must land before exit
+    // the loads in flight must land before exit
     if (lane == 0) {
-      for (int j = (n_kv > 2 ? n_kv - 2 : 0); j < n_kv; ++j)
-        if (!mbar_wait(&B->kv_full[j & 1], (j >> 1) & 1)) report(p.status, kDevTimeout);
+      const int first = n_kv > kStages ? n_kv - kStages : 0;
+      for (int j = first; j < n_kv; ++j)
+        if (!mbar_wait(&B->kv_full[j % kStages], (j / kStages) & 1))
+          report(p.status, kDevTimeout);
       if (!mbar_wait(&B->q_full, 0)) report(p.status, kDevTimeout);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == C::kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t q_addr = smem_addr(smem + kQOff);
-      bool ok = wait_or_abort(&B->q_full, 0, B, p);
-      int issued_pv = 0;
-      for (int j = 0; ok && j <= n_kv; ++j) {
-        if (j < n_kv) {
-          const int st = j & 1;
-          ok = wait_or_abort(&B->kv_full[st], (j >> 1) & 1, B, p);
-          if (ok && j >= 2) ok = wait_or_abort(&B->s_free[st], ((j - 2) >> 1) & 1, B, p);
+      const uint32_t q_addr = smem_addr(smem + C::kQOff);
+      auto issue_qk = [&](int j, int hh) {
+        const uint32_t k_addr = smem_addr(smem + C::kKOff + (j % kStages) * kTileBytes);
+        const uint32_t qa = q_addr + hh * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_f16_ss(tmem + C::s_col(hh), desc_sw128(qa + kk * 32, 16, 1024),
+                     desc_sw128(k_addr + kk * 32, 16, 1024), kIdescQK, kk > 0);
+        mma_commit(&B->s_full[hh]);
+      };
+      bool ok = wait_or_abort(&B->q_full, 0, B, p) && wait_or_abort(&B->kv_full[0], 0, B, p);
+      if (ok) {
+        tc_fence_after();
+        for (int hh = 0; hh < NH; ++hh) issue_qk(0, hh);
+      }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int st = j % kStages;
+        for (int hh = 0; ok && hh < NH; ++hh) {
+          ok = wait_or_abort(&B->p_full[hh], j & 1, B, p) &&
+               wait_or_abort(&B->v_ready[st], (j / kStages) & 1, B, p);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t k_addr = smem_addr(smem + kKOff + st * kTileBytes);
+          const uint32_t v_addr = smem_addr(smem + C::kVOff + st * kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            mma_f16_ss(tmem + st * kBN, desc_sw128(q_addr + kk * 32, 16, 1024),
-                       desc_sw128(k_addr + kk * 32, 16, 1024), kIdescQK, kk > 0);
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_f16_ts(tmem + C::o_col(hh), tmem + C::p_col(hh) + kk * 8,
+                       desc_sw128(v_addr + kk * 2048, 16, 1024), kIdescPV, (j > 0 || kk > 0));
+          mma_commit(&B->pv_done[hh]);
+          if (hh == NH - 1) mma_commit(&B->kv_empty[st]);
+          if (j + 1 < n_kv) {
+            if (hh == 0) ok = wait_or_abort(&B->kv_full[(j + 1) % kStages],
+                                            ((j + 1) / kStages) & 1, B, p);
+            if (!ok) break;
+            tc_fence_after();
+            issue_qk(j + 1, hh);
           }
-          mma_commit(&B->s_full[st]);
-        }
-        if (j >= 1) {
-          const int jp = j - 1;
-          const int st = jp & 1;
-          ok = wait_or_abort(&B->p_full[st], (jp >> 1) & 1, B, p);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t p_addr = smem_addr(smem + kPOff + st * 2 * kTileBytes);
-          const uint32_t v_addr = smem_addr(smem + kVOff + st * kTileBytes);
-#pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            mma_f16_ss(tmem + kTmemO,
-                       desc_sw128(p_addr + (kk >> 2) * kTileBytes + (kk & 3) * 32, 16, 1024),
-                       desc_sw128(v_addr + kk * 2048, 16, 1024), kIdescPV, (jp > 0 || kk > 0));
-          }
-          mma_commit(&B->pv_done[st]);
-          mma_commit(&B->kv_empty[st]);
-          issued_pv = j;
         }
       }
       // every MMA issued must be complete before TMEM is released
-      (void)issued_pv;
       mma_commit(&B->mma_done);
       if (!mbar_wait(&B->mma_done, 0)) report(p.status, kDevTimeout);
     }
   } else {
     // ------------------------------------------------------------- softmax
-    const int r = threadIdx.x;                          // row == TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int hh = warp >> 2;                           // head of this warpgroup
+    const int wi = warp & 3;                            // TMEM lane quadrant
+    const int r = wi * 32 + lane;                       // row == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(wi * 32) << 16;
+    const uint32_t s_addr = tmem + lane_off + C::s_col(hh);
+    const uint32_t o_addr = tmem + lane_off + C::o_col(hh);
+    const uint32_t p_addr = tmem + lane_off + C::p_col(hh);
     const int qpos = pos_first + r;
+    // this thread's share of the V conversion: NH warpgroups split the rows
+    const int vrows = kBN / NH;
+    const int vrow = hh * vrows + (NH == 2 ? (r >> 1) : r);
+    const int vchunk0 = NH == 2 ? (r & 1) * 4 : 0;
+    const int vchunks = NH == 2 ? 4 : 8;
+    const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
     float m_used = -INFINITY;
-    float l = 0.f;
+    float2 l2 = make_float2(0.f, 0.f);
     bool ok = true;
     for (int j = 0; j < n_kv && ok; ++j) {
-      const int sb = j & 1;
-      ok = wait_or_abort(&B->s_full[sb], (j >> 1) & 1, B, p);
+      const int st = j % kStages;
+      const int key0 = j * kBN;
+      // --- V tile j: bf16 -> fp16 in place, keys past the context -> 0
+      ok = wait_or_abort(&B->kv_full[st], (j / kStages) & 1, B, p);
+      if (__any_sync(kFull, !ok)) { ok = false; break; }
+      {
+        uint8_t* vr = smem + C::kVOff + st * kTileBytes + vrow * 128;
+        const bool key_ok = key0 + vrow < ctx;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (i >= vchunks) break;
+          const int chunk = (vchunk0 + i) ^ (vrow & 7);
+          uint4 w = *reinterpret_cast<const uint4*>(vr + chunk * 16);
+          if (key_ok) {
+            w.x = bf16x2_to_half2(w.x);
+            w.y = bf16x2_to_half2(w.y);
+            w.z = bf16x2_to_half2(w.z);
+            w.w = bf16x2_to_half2(w.w);
+          } else {
+            w = make_uint4(0, 0, 0, 0);
+          }
+          *reinterpret_cast<uint4*>(vr + chunk * 16) = w;
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B->v_ready[st]);
+      }
+      // --- S tile j
+      ok = wait_or_abort(&B->s_full[hh], j & 1, B, p);
       if (__any_sync(kFull, !ok)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_off + sb * kBN + c * 32, sr[c]);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&B->s_free[sb]);
-
-      const int key0 = j * kBN;
+      // pass 1: tile maximum of the scaled scores, read 64 columns at a time.
+      // On tiles that need the causal or context mask the scores are scaled
+      // first and masked to -inf (masking raw scores would give -inf * 0 =
+      // NaN for scale 0); elsewhere the maximum (minimum, for a negative
+      // scale) of the raw scores is scaled.
       const bool masked = (key0 + kBN - 1 > pos_first) || (key0 + kBN > ctx);
       const int limit = min(qpos, ctx - 1) - key0;     // last visible column
-      float mx = -INFINITY;
+      const bool pos_scale = p.scale_log2 >= 0.f;
+      float mt = masked || pos_scale ? -INFINITY : INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int half = 0; half < 2; ++half) {
+        uint32_t sr[2][32];
+        tmem_ld32(s_addr + half * 64, sr[0]);
+        tmem_ld32(s_addr + half * 64 + 32, sr[1]);
+        tmem_ld_wait();
+        if (masked) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float v = __uint_as_float(sr[c][e]) * p.scale_log2;
-          if (masked && (c * 32 + e) > limit) v = -INFINITY;
-          sr[c][e] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              float v = __uint_as_float(sr[c][e]) * p.scale_log2;
+              if (half * 64 + c * 32 + e > limit) v = -INFINITY;
+              mt = fmaxf(mt, v);
+            }
+        } else if (pos_scale) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; e += 2)
+              mt = max3(mt, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; e += 2)
+              mt = min3(mt, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
         }
-      const float m_new = fmaxf(m_used, mx);
+      }
+      if (!masked) mt *= p.scale_log2;
+      const float m_new = fmaxf(m_used, mt);
       const bool need = m_new > m_used + kRescaleLog2;
       if (__any_sync(kFull, need)) {
         const float f = need ? ex2(m_used - m_new) : 1.0f;
         if (j > 0) {
           // O *= f needs the previous P.V to have landed in TMEM
-          ok = wait_or_abort(&B->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, B, p);
+          ok = wait_or_abort(&B->pv_done[hh], (j - 1) & 1, B, p);
           if (__any_sync(kFull, !ok)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t o[32];
-            tmem_ld32(tmem + lane_off + kTmemO + c * 32, o);
+            tmem_ld32(o_addr + c * 32, o);
             tmem_ld_wait();
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-            tmem_st32(tmem + lane_off + kTmemO + c * 32, o);
+            tmem_st32(o_addr + c * 32, o);
           }
           tmem_st_wait();
         }
         if (need) {
           m_used = m_new;
-          l *= f;
+          l2.x *= f;
+          l2.y *= f;
         }
       }
       const float mref = m_used == -INFINITY ? 0.f : m_used;
-      if (j >= 2) {   // P buffer sb is free once P.V of tile j-2 completed
-        ok = wait_or_abort(&B->pv_done[sb], ((j - 2) >> 1) & 1, B, p);
+      const float2 nm2 = make_float2(-mref, -mref);
+      // P_h of tile j-1 must have been consumed by its P.V before it is overwritten
+      if (j >= 1) {
+        ok = wait_or_abort(&B->pv_done[hh], (j - 1) & 1, B, p);
         if (__any_sync(kFull, !ok)) { ok = false; break; }
+        tc_fence_after();
       }
-      uint8_t* pbuf = smem + kPOff + sb * 2 * kTileBytes;
+      // pass 2: P = 2^(S * scale * log2e - m), 32 columns at a time, fp16 into TMEM
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const int c = q >> 2, e0 = (q & 3) * 8;
-        float pv[8];
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sr[32];
+        tmem_ld32(s_addr + c * 32, sr);
+        tmem_ld_wait();
+        uint32_t ph[16];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          pv[e] = ex2(__uint_as_float(sr[c][e0 + e]) - mref);
-          l += pv[e];
+        for (int e = 0; e < 32; e += 2) {
+          float2 x = make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+          x = __ffma2_rn(x, sl2, nm2);
+          if (masked) {
+            if (c * 32 + e > limit) x.x = -INFINITY;
+            if (c * 32 + e + 1 > limit) x.y = -INFINITY;
+          }
+          const float2 pv = make_float2(ex2(x.x), ex2(x.y));
+          l2 = __fadd2_rn(l2, pv);
+          ph[e / 2] = pack_half2(pv.x, pv.y);
         }
-        const uint4 w = make_uint4(pack_half2(pv[0], pv[1]), pack_half2(pv[2], pv[3]),
-                                   pack_half2(pv[4], pv[5]), pack_half2(pv[6], pv[7]));
-        const int region = q >> 3, chunk = q & 7;
-        *reinterpret_cast<uint4*>(pbuf + region * kTileBytes + r * 128 +
-                                  ((chunk ^ (r & 7)) << 4)) = w;
+        tmem_st16(p_addr + c * 16, ph);
       }
-      // V tile j: bf16 -> fp16 in place; keys past the context become zero
-      ok = wait_or_abort(&B->kv_full[sb], (j >> 1) & 1, B, p);
-      if (__any_sync(kFull, !ok)) { ok = false; break; }
-      uint8_t* vrow = smem + kVOff + sb * kTileBytes + r * 128;
-      const bool key_ok = key0 + r < ctx;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int chunk = i ^ (r & 7);
-        uint4 w = *reinterpret_cast<const uint4*>(vrow + chunk * 16);
-        if (key_ok) {
-          w.x = bf16x2_to_half2(w.x);
-          w.y = bf16x2_to_half2(w.y);
-          w.z = bf16x2_to_half2(w.z);
-          w.w = bf16x2_to_half2(w.w);
-        } else {
-          w = make_uint4(0, 0, 0, 0);
-        }
-        *reinterpret_cast<uint4*>(vrow + chunk * 16) = w;
-      }
-      fence_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&B->p_full[sb]);
+      if (lane == 0) mbar_arrive(&B->p_full[hh]);
     }
     if (ok) {
       const int jl = n_kv - 1;
-      ok = wait_or_abort(&B->pv_done[jl & 1], (jl >> 1) & 1, B, p);
+      ok = wait_or_abort(&B->pv_done[hh], jl & 1, B, p);
     }
     if (!__any_sync(kFull, !ok)) {
       tc_fence_after();
       uint32_t o[2][32];
-      tmem_ld32(tmem + lane_off + kTmemO, o[0]);
-      tmem_ld32(tmem + lane_off + kTmemO + 32, o[1]);
+      tmem_ld32(o_addr, o[0]);
+      tmem_ld32(o_addr + 32, o[1]);
       tmem_ld_wait();
       if (r < rows) {
-        const float inv = 1.0f / l;
+        const float inv = 1.0f / (l2.x + l2.y);
         float4* dst = reinterpret_cast<float4*>(
-            p.out + (static_cast<long long>(q0 + row0 + r) * p.hq + h) * kD);
+            p.out + (static_cast<long long>(q0 + row0 + r) * p.hq + h0 + hh) * kD);
 #pragma unroll
         for (int c = 0; c < 2; ++c)
 #pragma unroll
@@ -391,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
@@ -420,6 +502,18 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+template <int NH>
+cudaError_t launch_nh(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                      const Params& p, int num_seqs, cudaStream_t stream) {
+  using C = Cfg<NH>;
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<NH>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.n_qtiles, p.hq / NH, num_seqs);
+  return launch_pdl(prefill_kernel<NH>, grid, dim3(C::kThreads), C::kSmemBytes, stream, tq, tk,
+                    tv, p);
 }
 
 }  // namespace
@@ -462,12 +556,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.n_qtiles = (a.max_q_len + kBM - 1) / kBM;
   p.scale_log2 = a.scale * kLog2e;
   p.status = a.status;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kSmemBytes);
-  if (e != cudaSuccess) return e;
-  dim3 grid(p.n_qtiles, a.num_q_heads, a.num_seqs);
-  prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  if (p.group >= 2) return launch_nh<2>(tq, tk, tv, p, a.num_seqs, stream);
+  return launch_nh<1>(tq, tk, tv, p, a.num_seqs, stream);
 }
 
 }  // namespace tvl
