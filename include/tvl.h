@@ -67,7 +67,8 @@ typedef enum {
   TVL_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. head_dim 128)  */
   TVL_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required     */
   TVL_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed              */
-  TVL_ERR_DEVICE_CHECK = 5   /* a kernel found bad metadata (status word set)  */
+  TVL_ERR_DEVICE_CHECK = 5,  /* a kernel found bad metadata (status word set)  */
+  TVL_ERR_OUT_OF_BLOCKS = 6  /* allocator: the block pool cannot cover a call  */
 } tvl_status;
 
 /* Bits of the device status word (tvl_get_device_status). */
@@ -189,6 +190,80 @@ tvl_status tvl_paged_attention_decode_noalloc(
     int num_q_heads, int num_kv_heads, int head_dim, int block_size,
     int num_blocks, int max_blocks_per_seq, float scale, int partition_size,
     void* stream);
+
+/*
+ * Block copy [nano-vLLM guide ch. 7 "Prefix Caching": sequences that share a
+ * prefix share its blocks until one of them writes into a shared block]:
+ * for i in [0, n), physical block dst[i] of both caches becomes a copy of
+ * block src[i] (bs * Hkv * D bf16 values each), bit-exact.  The pairs must
+ * not overlap (no block is both a source and a destination).  Ids outside
+ * [0, NB) are skipped and set TVL_DEV_BAD_BLOCK_ID.
+ *   k_cache, v_cache : bf16 [NB, bs, Hkv, D] (device, in place)
+ *   src, dst         : int32 [n] (device)
+ */
+tvl_status tvl_copy_blocks(void* k_cache, void* v_cache, const int32_t* src,
+                           const int32_t* dst, int n, int num_kv_heads,
+                           int head_dim, int block_size, int num_blocks,
+                           void* stream);
+
+/*
+ * Host block allocator: the CPU control plane that hands out the physical
+ * blocks and slots the kernels read [nano-vLLM guide ch. 2 (control plane vs
+ * data plane), ch. 4 "PagedAttention" (block allocator, no fragmentation
+ * beyond the last block of a sequence), ch. 5 "The Scheduler" (continuous
+ * batching), ch. 7 "Prefix Caching" (shared prefix blocks)].  Host memory
+ * only; calls on one allocator are serialised internally.  Every call is
+ * all-or-nothing.
+ */
+typedef struct tvl_allocator tvl_allocator;
+
+typedef struct {
+  int num_blocks;        /* pool size                                        */
+  int free_blocks;       /* blocks with no owner                             */
+  int live_sequences;
+  int shared_blocks;     /* blocks owned by more than one sequence           */
+  long long tokens;      /* sum of the live sequences' lengths               */
+  long long slack_slots; /* sum over sequences of unused slots in own blocks */
+} tvl_allocator_stats_t;
+
+/* A pool of num_blocks blocks of block_size tokens; *out owns it. */
+tvl_status tvl_allocator_create(int num_blocks, int block_size,
+                                tvl_allocator** out);
+void tvl_allocator_destroy(tvl_allocator* allocator);
+/* A new empty sequence; its id goes to *seq (ids of freed sequences are
+ * reused). */
+tvl_status tvl_allocator_new_sequence(tvl_allocator* allocator, int* seq);
+/* A new sequence that shares every block (and the length) of `parent`. */
+tvl_status tvl_allocator_fork(tvl_allocator* allocator, int parent, int* child);
+/* Reserves the next num_tokens positions of `seq` and writes their cache
+ * slots (block * bs + offset) to slots[0..num_tokens).  New blocks are taken
+ * from the pool; if the sequence's last block is shared and partly filled it
+ * is first replaced by a private copy, and the (old, new) pair is queued for
+ * tvl_allocator_take_copies -- run those copies (tvl_copy_blocks) before
+ * writing to the returned slots.  TVL_ERR_OUT_OF_BLOCKS if the pool cannot
+ * cover the call (nothing changes). */
+tvl_status tvl_allocator_append(tvl_allocator* allocator, int seq,
+                                int num_tokens, int32_t* slots);
+/* Releases the sequence's hold on its blocks and retires its id. */
+tvl_status tvl_allocator_free_sequence(tvl_allocator* allocator, int seq);
+tvl_status tvl_allocator_context_len(tvl_allocator* allocator, int seq,
+                                     long long* len);
+/* Row i of block_tables [n, max_blocks_per_seq] (host, -1 padded) and
+ * context_lens[i] describe sequence seqs[i]: the arguments of the decode and
+ * prefill calls for that batch. */
+tvl_status tvl_allocator_build_tables(tvl_allocator* allocator,
+                                      const int* seqs, int n,
+                                      int max_blocks_per_seq,
+                                      int32_t* block_tables,
+                                      int32_t* context_lens);
+/* Moves the queued copy-on-write pairs into src/dst (host, `capacity`
+ * entries) and their number into *count.  If capacity is too small nothing is
+ * moved, *count holds the number needed and TVL_ERR_INVALID_ARG is
+ * returned. */
+tvl_status tvl_allocator_take_copies(tvl_allocator* allocator, int32_t* src,
+                                     int32_t* dst, int capacity, int* count);
+tvl_status tvl_allocator_stats(tvl_allocator* allocator,
+                               tvl_allocator_stats_t* stats);
 
 /* Static description of a status code. */
 const char* tvl_status_string(tvl_status status);

@@ -19,7 +19,7 @@ import threading
 import torch
 
 __all__ = [
-    "TvlError", "paged_kv_write", "paged_attention_decode",
+    "TvlError", "paged_kv_write", "paged_attention_decode", "copy_blocks", "BlockAllocator",
     "paged_attention_decode_workspace_size", "paged_attention_prefill", "get_device_status",
     "version", "library_path", "DEV_BAD_SLOT", "DEV_BAD_BLOCK_ID", "DEV_BAD_CONTEXT_LEN",
     "DEV_BAD_QUERY_LEN", "DEV_TIMEOUT",
@@ -28,7 +28,8 @@ __all__ = [
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libtvl.so")
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_CHECK = range(6)
+(OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_CHECK,
+ ERR_OUT_OF_BLOCKS) = range(7)
 DEV_BAD_SLOT, DEV_BAD_BLOCK_ID, DEV_BAD_CONTEXT_LEN, DEV_BAD_QUERY_LEN, DEV_TIMEOUT = (
     0x1, 0x2, 0x4, 0x8, 0x10)
 
@@ -76,6 +77,26 @@ def _load():
             lib.tvl_last_error.restype = ctypes.c_char_p
             lib.tvl_version.argtypes = []
             lib.tvl_version.restype = I
+            lib.tvl_copy_blocks.argtypes = [P, P, P, P, I, I, I, I, I, P]
+            lib.tvl_copy_blocks.restype = I
+            I32P = ctypes.POINTER(ctypes.c_int32)
+            IP = ctypes.POINTER(ctypes.c_int)
+            lib.tvl_allocator_create.argtypes = [I, I, ctypes.POINTER(P)]
+            lib.tvl_allocator_destroy.argtypes = [P]
+            lib.tvl_allocator_destroy.restype = None
+            lib.tvl_allocator_new_sequence.argtypes = [P, IP]
+            lib.tvl_allocator_fork.argtypes = [P, I, IP]
+            lib.tvl_allocator_append.argtypes = [P, I, I, I32P]
+            lib.tvl_allocator_free_sequence.argtypes = [P, I]
+            lib.tvl_allocator_context_len.argtypes = [P, I, ctypes.POINTER(ctypes.c_longlong)]
+            lib.tvl_allocator_build_tables.argtypes = [P, IP, I, I, I32P, I32P]
+            lib.tvl_allocator_take_copies.argtypes = [P, I32P, I32P, I, IP]
+            lib.tvl_allocator_stats.argtypes = [P, ctypes.c_void_p]
+            for name in ("tvl_allocator_create", "tvl_allocator_new_sequence", "tvl_allocator_fork",
+                         "tvl_allocator_append", "tvl_allocator_free_sequence",
+                         "tvl_allocator_context_len", "tvl_allocator_build_tables",
+                         "tvl_allocator_take_copies", "tvl_allocator_stats"):
+                getattr(lib, name).restype = I
             _lib = lib
     return _lib
 
@@ -215,3 +236,110 @@ def get_device_status(stream=None) -> int:
     if rc not in (OK, ERR_DEVICE_CHECK):
         _check(rc)
     return int(bits.value)
+
+
+def copy_blocks(k_cache, v_cache, src, dst, stream=None) -> None:
+    """Physical block dst[i] of both caches <- block src[i] (int32 CUDA
+    tensors [n]); bit-exact; the pairs must not overlap."""
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    dev = k_cache.device
+    _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _need(src, "src", torch.int32, 1, dev)
+    _need(dst, "dst", torch.int32, 1, dev)
+    if src.shape != dst.shape:
+        raise ValueError("src and dst differ in length")
+    nb, bs, hkv, d = k_cache.shape
+    with torch.cuda.device(dev):
+        _check(_load().tvl_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(src), _ptr(dst),
+                                       src.numel(), hkv, d, bs, nb, _stream(stream)))
+
+
+class _Stats(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int), ("free_blocks", ctypes.c_int),
+                ("live_sequences", ctypes.c_int), ("shared_blocks", ctypes.c_int),
+                ("tokens", ctypes.c_longlong), ("slack_slots", ctypes.c_longlong)]
+
+
+class BlockAllocator:
+    """Host block allocator of libtvl (tvl_allocator_*): hands out physical
+    blocks and cache slots, shares blocks between forked sequences and queues
+    copy-on-write block copies.  Host memory only."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        import numpy as np  # noqa: F401
+
+        self._lib = _load()
+        self._h = ctypes.c_void_p()
+        _check(self._lib.tvl_allocator_create(num_blocks, block_size, ctypes.byref(self._h)))
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def close(self):
+        if self._h:
+            self._lib.tvl_allocator_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def new_sequence(self) -> int:
+        out = ctypes.c_int(0)
+        _check(self._lib.tvl_allocator_new_sequence(self._h, ctypes.byref(out)))
+        return out.value
+
+    def fork(self, parent: int) -> int:
+        out = ctypes.c_int(0)
+        _check(self._lib.tvl_allocator_fork(self._h, parent, ctypes.byref(out)))
+        return out.value
+
+    def append(self, seq: int, num_tokens: int):
+        import numpy as np
+
+        slots = np.zeros(max(num_tokens, 1), dtype=np.int32)
+        _check(self._lib.tvl_allocator_append(
+            self._h, seq, num_tokens, slots.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))))
+        return slots[:num_tokens]
+
+    def free(self, seq: int) -> None:
+        _check(self._lib.tvl_allocator_free_sequence(self._h, seq))
+
+    def context_len(self, seq: int) -> int:
+        out = ctypes.c_longlong(0)
+        _check(self._lib.tvl_allocator_context_len(self._h, seq, ctypes.byref(out)))
+        return int(out.value)
+
+    def build_tables(self, seqs, max_blocks_per_seq: int):
+        import numpy as np
+
+        ids = np.ascontiguousarray(seqs, dtype=np.intc)
+        n = ids.shape[0]
+        tables = np.zeros((max(n, 1), max_blocks_per_seq), dtype=np.int32)
+        ctx = np.zeros(max(n, 1), dtype=np.int32)
+        _check(self._lib.tvl_allocator_build_tables(
+            self._h, ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), n, max_blocks_per_seq,
+            tables.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+            ctx.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))))
+        return tables[:n], ctx[:n]
+
+    def take_copies(self):
+        import numpy as np
+
+        count = ctypes.c_int(0)
+        rc = self._lib.tvl_allocator_take_copies(self._h, None, None, 0, ctypes.byref(count))
+        if rc == OK and count.value == 0:
+            return np.zeros(0, np.int32), np.zeros(0, np.int32)
+        src = np.zeros(count.value, dtype=np.int32)
+        dst = np.zeros(count.value, dtype=np.int32)
+        _check(self._lib.tvl_allocator_take_copies(
+            self._h, src.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+            dst.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), count.value,
+            ctypes.byref(count)))
+        return src[:count.value], dst[:count.value]
+
+    def stats(self) -> dict:
+        st = _Stats()
+        _check(self._lib.tvl_allocator_stats(self._h, ctypes.byref(st)))
+        return {name: getattr(st, name) for name, _ in _Stats._fields_}

@@ -139,6 +139,7 @@ const char* tvl_status_string(tvl_status status) {
     case TVL_ERR_WORKSPACE: return "workspace missing or too small";
     case TVL_ERR_CUDA: return "CUDA error";
     case TVL_ERR_DEVICE_CHECK: return "device-side metadata check failed";
+    case TVL_ERR_OUT_OF_BLOCKS: return "block pool exhausted";
   }
   return "unknown status";
 }
@@ -198,6 +199,34 @@ tvl_status tvl_paged_kv_write(const void* k_new, const void* v_new, void* k_cach
   a.status = word;
   cudaError_t e = tvl::launch_kv_write(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kv_write launch");
+  return TVL_OK;
+}
+
+tvl_status tvl_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst,
+                           int n, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                           void* stream) {
+  if (n < 0) return fail(TVL_ERR_INVALID_ARG, "n %d < 0", n);
+  if (num_kv_heads <= 0 || block_size <= 0 || num_blocks <= 0)
+    return fail(TVL_ERR_INVALID_ARG, "num_kv_heads, block_size and num_blocks must be positive");
+  if (head_dim != 64) return fail(TVL_ERR_UNSUPPORTED, "head_dim %d (supported: 64)", head_dim);
+  if (n == 0) return TVL_OK;
+  if (!k_cache || !v_cache || !src || !dst) return fail(TVL_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(k_cache) || !aligned16(v_cache))
+    return fail(TVL_ERR_INVALID_ARG, "cache pointers must be 16-byte aligned");
+  uint32_t* word = nullptr;
+  tvl_status st = status_word(&word);
+  if (st != TVL_OK) return st;
+  tvl::CopyBlocksArgs a;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.src = src;
+  a.dst = dst;
+  a.n = n;
+  a.block_bytes = 2LL * block_size * num_kv_heads * head_dim;
+  a.num_blocks = num_blocks;
+  a.status = word;
+  cudaError_t e = tvl::launch_copy_blocks(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "copy_blocks launch");
   return TVL_OK;
 }
 

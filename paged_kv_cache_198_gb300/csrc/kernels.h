@@ -21,6 +21,18 @@ struct KvWriteArgs {
 };
 cudaError_t launch_kv_write(const KvWriteArgs& a, cudaStream_t stream);
 
+struct CopyBlocksArgs {
+  void* k_cache;
+  void* v_cache;
+  const int32_t* src;
+  const int32_t* dst;
+  int n;
+  long long block_bytes;   // bs * Hkv * D * 2
+  int num_blocks;
+  uint32_t* status;
+};
+cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream);
+
 // Partial results of the decode (split-K) live in a workspace of `records`
 // records; record r, query head h: m (log2 domain running max used),
 // l (sum of exp2), acc[D] (unnormalised weighted sum of V).

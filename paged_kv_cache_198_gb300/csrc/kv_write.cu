@@ -46,7 +46,35 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   }
 }
 
+// One CTA per (pair, cache): block dst of the cache becomes a copy of block
+// src, 16-byte vectors.
+__global__ void __launch_bounds__(256)
+    copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                       const int32_t* __restrict__ src, const int32_t* __restrict__ dst,
+                       long long block_vecs, int num_blocks, uint32_t* status) {
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int i = blockIdx.x;
+  const int from = src[i];
+  const int to = dst[i];
+  if (from < 0 || from >= num_blocks || to < 0 || to >= num_blocks) {
+    if (threadIdx.x == 0) report(status, TVL_DEV_BAD_BLOCK_ID);
+    return;
+  }
+  uint4* cache = blockIdx.y == 0 ? k_cache : v_cache;
+  const uint4* s = cache + from * block_vecs;
+  uint4* d = cache + to * block_vecs;
+  for (long long v = threadIdx.x; v < block_vecs; v += blockDim.x) d[v] = s[v];
+}
+
 }  // namespace
+
+cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream) {
+  if (a.n == 0) return cudaSuccess;
+  return launch_pdl(copy_blocks_kernel, dim3(a.n, 2), dim3(256), 0, stream,
+                    static_cast<uint4*>(a.k_cache), static_cast<uint4*>(a.v_cache), a.src, a.dst,
+                    a.block_bytes / 16, a.num_blocks, a.status);
+}
 
 cudaError_t launch_kv_write(const KvWriteArgs& a, cudaStream_t stream) {
   if (a.num_tokens == 0) return cudaSuccess;

@@ -14,13 +14,14 @@
 //   0..4NH-1  softmax, one warpgroup per head: thread r owns query row r
 //             (TMEM lane r).  Per 128-key tile it converts its share of the V
 //             tile bf16 -> fp16 in place (exact for |v| >= 2^-14; keys past
-//             the context become 0), finds the row maximum of S, keeps a
-//             running maximum that moves only when a score exceeds it by more
-//             than 2^8 (exact: one reference maximum scales numerator and
-//             denominator; O in TMEM is rescaled when it moves), computes
-//             P = 2^(S*scale*log2e - m) with packed fp32x2 arithmetic and
-//             stores it as fp16 into TMEM; at the end it normalises O and
-//             writes it out;
+//             the context become 0) while its S loads are in flight, then
+//             computes P = 2^(S*scale*log2e - m) with packed fp32x2 arithmetic
+//             against a running reference maximum m and stores it as fp16
+//             into TMEM.  m is set by the first tile and moved only on masked
+//             (diagonal / context-tail) tiles or when a tile's row sum shows
+//             that some P could overflow fp16; O in TMEM is rescaled when it
+//             moves (exact: one reference maximum scales numerator and
+//             denominator).  At the end it normalises O and writes it out;
 //   4NH       producer: TMA loads of the Q tiles and, per 128-key tile, one
 //             box of bs tokens x 64 dims per physical block (K and V) found
 //             through the block table -- the paged gather; blocks past the
@@ -310,15 +311,79 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
     const int vchunk0 = NH == 2 ? (r & 1) * 4 : 0;
     const int vchunks = NH == 2 ? 4 : 8;
     const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+    (void)kRescaleLog2;
     float m_used = -INFINITY;
     float2 l2 = make_float2(0.f, 0.f);
     bool ok = true;
+    // P for 64 columns [col0, col0 + 64) of this row from scores already in
+    // registers: p = 2^(s * scale * log2e - m), fp16 pairs into TMEM columns
+    // P + col0 / 2; returns the sum of the p (fp32, before rounding).
+    auto emit_p = [&](const uint32_t (&sr)[2][32], int col0, float mref, bool masked,
+                      int limit) -> float2 {
+      const float2 nm2 = make_float2(-mref, -mref);
+      float2 sum = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t ph[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float2 x = make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+          x = __ffma2_rn(x, sl2, nm2);
+          if (masked) {
+            if (col0 + c * 32 + e > limit) x.x = -INFINITY;
+            if (col0 + c * 32 + e + 1 > limit) x.y = -INFINITY;
+          }
+          const float2 pv = make_float2(ex2(x.x), ex2(x.y));
+          sum = __fadd2_rn(sum, pv);
+          ph[e / 2] = pack_half2(pv.x, pv.y);
+        }
+        tmem_st16(p_addr + col0 / 2 + c * 16, ph);
+      }
+      return sum;
+    };
+    // maximum of the scaled, masked scores of 64 columns in registers
+    auto tile_max = [&](const uint32_t (&sr)[2][32], int col0, bool masked, int limit) {
+      float mt = -INFINITY;
+      if (masked) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float v = __uint_as_float(sr[c][e]) * p.scale_log2;
+            if (col0 + c * 32 + e > limit) v = -INFINITY;
+            mt = fmaxf(mt, v);
+          }
+      } else if (p.scale_log2 >= 0.f) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            mt = max3(mt, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+        mt *= p.scale_log2;
+      } else {
+        float mn = INFINITY;
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            mn = min3(mn, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+        mt = mn * p.scale_log2;
+      }
+      return mt;
+    };
+
     for (int j = 0; j < n_kv && ok; ++j) {
       const int st = j % kStages;
       const int key0 = j * kBN;
-      // --- V tile j: bf16 -> fp16 in place, keys past the context -> 0
-      ok = wait_or_abort(&B->kv_full[st], (j / kStages) & 1, B, p);
+      ok = wait_or_abort(&B->kv_full[st], (j / kStages) & 1, B, p) &&
+           wait_or_abort(&B->s_full[hh], j & 1, B, p);
       if (__any_sync(kFull, !ok)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sa[2][32];                               // columns [0, 64)
+      tmem_ld32(s_addr, sa[0]);
+      tmem_ld32(s_addr + 32, sa[1]);
+      // --- while those loads fly: V tile j bf16 -> fp16 in place (keys past
+      // the context -> 0), this warpgroup's share of the rows
       {
         uint8_t* vr = smem + C::kVOff + st * kTileBytes + vrow * 128;
         const bool key_ok = key0 + vrow < ctx;
@@ -341,104 +406,80 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&B->v_ready[st]);
       }
-      // --- S tile j
-      ok = wait_or_abort(&B->s_full[hh], j & 1, B, p);
-      if (__any_sync(kFull, !ok)) { ok = false; break; }
-      tc_fence_after();
-      // pass 1: tile maximum of the scaled scores, read 64 columns at a time.
-      // On tiles that need the causal or context mask the scores are scaled
-      // first and masked to -inf (masking raw scores would give -inf * 0 =
-      // NaN for scale 0); elsewhere the maximum (minimum, for a negative
-      // scale) of the raw scores is scaled.
+      tmem_ld_wait();
+
+      // Tiles on the causal diagonal or past the context need the mask, and
+      // the first tile sets the running maximum: those take the exact path.
+      // Every other tile computes P against the running maximum directly and
+      // only falls back to the exact path if its row sum exceeds 60000: below
+      // that every P fits fp16 (max 65504), and the result is exact either
+      // way because one reference maximum scales numerator and denominator.
       const bool masked = (key0 + kBN - 1 > pos_first) || (key0 + kBN > ctx);
       const int limit = min(qpos, ctx - 1) - key0;     // last visible column
-      const bool pos_scale = p.scale_log2 >= 0.f;
-      float mt = masked || pos_scale ? -INFINITY : INFINITY;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t sr[2][32];
-        tmem_ld32(s_addr + half * 64, sr[0]);
-        tmem_ld32(s_addr + half * 64 + 32, sr[1]);
-        tmem_ld_wait();
-        if (masked) {
-#pragma unroll
-          for (int c = 0; c < 2; ++c)
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              float v = __uint_as_float(sr[c][e]) * p.scale_log2;
-              if (half * 64 + c * 32 + e > limit) v = -INFINITY;
-              mt = fmaxf(mt, v);
-            }
-        } else if (pos_scale) {
-#pragma unroll
-          for (int c = 0; c < 2; ++c)
-#pragma unroll
-            for (int e = 0; e < 32; e += 2)
-              mt = max3(mt, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 2; ++c)
-#pragma unroll
-            for (int e = 0; e < 32; e += 2)
-              mt = min3(mt, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-        }
-      }
-      if (!masked) mt *= p.scale_log2;
-      const float m_new = fmaxf(m_used, mt);
-      const bool need = m_new > m_used + kRescaleLog2;
-      if (__any_sync(kFull, need)) {
-        const float f = need ? ex2(m_used - m_new) : 1.0f;
-        if (j > 0) {
-          // O *= f needs the previous P.V to have landed in TMEM
-          ok = wait_or_abort(&B->pv_done[hh], (j - 1) & 1, B, p);
-          if (__any_sync(kFull, !ok)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t o[32];
-            tmem_ld32(o_addr + c * 32, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-            tmem_st32(o_addr + c * 32, o);
-          }
-          tmem_st_wait();
-        }
-        if (need) {
-          m_used = m_new;
-          l2.x *= f;
-          l2.y *= f;
-        }
-      }
-      const float mref = m_used == -INFINITY ? 0.f : m_used;
-      const float2 nm2 = make_float2(-mref, -mref);
-      // P_h of tile j-1 must have been consumed by its P.V before it is overwritten
-      if (j >= 1) {
+      bool exact = masked || j == 0;
+      float2 tsum = make_float2(0.f, 0.f);
+      if (!exact) {
+        // P_h of tile j-1 must have been consumed before it is overwritten
         ok = wait_or_abort(&B->pv_done[hh], (j - 1) & 1, B, p);
         if (__any_sync(kFull, !ok)) { ok = false; break; }
         tc_fence_after();
-      }
-      // pass 2: P = 2^(S * scale * log2e - m), 32 columns at a time, fp16 into TMEM
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sr[32];
-        tmem_ld32(s_addr + c * 32, sr);
+        tsum = emit_p(sa, 0, m_used, false, 0);
+        uint32_t sb[2][32];
+        tmem_ld32(s_addr + 64, sb[0]);
+        tmem_ld32(s_addr + 96, sb[1]);
         tmem_ld_wait();
-        uint32_t ph[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float2 x = make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
-          x = __ffma2_rn(x, sl2, nm2);
-          if (masked) {
-            if (c * 32 + e > limit) x.x = -INFINITY;
-            if (c * 32 + e + 1 > limit) x.y = -INFINITY;
-          }
-          const float2 pv = make_float2(ex2(x.x), ex2(x.y));
-          l2 = __fadd2_rn(l2, pv);
-          ph[e / 2] = pack_half2(pv.x, pv.y);
+        tsum = __fadd2_rn(tsum, emit_p(sb, 64, m_used, false, 0));
+        exact = __any_sync(kFull, tsum.x + tsum.y > 60000.f);   // < fp16 max 65504
+        if (exact) {
+          tmem_ld32(s_addr, sa[0]);
+          tmem_ld32(s_addr + 32, sa[1]);
+          tmem_ld_wait();
         }
-        tmem_st16(p_addr + c * 16, ph);
       }
+      if (exact) {
+        // one half of the scores in registers at a time
+        const float ma = tile_max(sa, 0, masked, limit);
+        uint32_t sb[2][32];
+        tmem_ld32(s_addr + 64, sb[0]);
+        tmem_ld32(s_addr + 96, sb[1]);
+        tmem_ld_wait();
+        const float mt = fmaxf(ma, tile_max(sb, 64, masked, limit));
+        const float m_new = fmaxf(m_used, mt);
+        const bool need = m_new > m_used;
+        if (j > 0) {
+          // O *= f (when the maximum moved) and the P buffer reuse both need
+          // the previous P.V to have landed
+          ok = wait_or_abort(&B->pv_done[hh], (j - 1) & 1, B, p);
+          if (__any_sync(kFull, !ok)) { ok = false; break; }
+          tc_fence_after();
+        }
+        if (__any_sync(kFull, need)) {
+          const float f = need ? ex2(m_used - m_new) : 1.0f;
+          if (j > 0) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              uint32_t o[32];
+              tmem_ld32(o_addr + c * 32, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+              tmem_st32(o_addr + c * 32, o);
+            }
+          }
+          if (need) {
+            m_used = m_new;
+            l2.x *= f;
+            l2.y *= f;
+          }
+        }
+        const float mref = m_used == -INFINITY ? 0.f : m_used;
+        tsum = emit_p(sb, 64, mref, masked, limit);
+        tmem_ld32(s_addr, sa[0]);
+        tmem_ld32(s_addr + 32, sa[1]);
+        tmem_ld_wait();
+        tsum = __fadd2_rn(tsum, emit_p(sa, 0, mref, masked, limit));
+      }
+      l2 = __fadd2_rn(l2, tsum);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
