@@ -98,6 +98,31 @@ tvl_status tvl_paged_kv_write(const void* k_new, const void* v_new,
                               int num_blocks, void* stream);
 
 /*
+ * Rotary position embedding fused into the paged KV write [tiny-vllm README,
+ * curriculum "RoPE" and "Paged KV cache"; Tiny-vLLM digest, "Core
+ * Mechanics"]: for every token t, each head vector of q[t] (in place, when q
+ * is not NULL) and of k_new[t] has its pairs (x_i, x_{i+D/2}), i < D/2,
+ * rotated by the angle a = positions[t] * rope_theta^(-2i/D):
+ *   x_i <- x_i cos a - x_{i+D/2} sin a,  x_{i+D/2} <- x_{i+D/2} cos a + x_i sin a,
+ * rounded to bf16 (the angle is reduced in double precision, the rotation is
+ * fp32).  Then, for slot_mapping[t] >= 0, the rotated K row and the V row are
+ * stored at that slot exactly as tvl_paged_kv_write does (negative slots:
+ * q is still rotated, nothing is stored).  k_new and v_new are not modified.
+ *   q        : bf16 [T, Hq, D] or NULL (device, rotated in place)
+ *   positions: int32 [T], absolute token positions >= 0 (device)
+ * Each result is within one bf16 ulp of the double-precision definition plus
+ * the fp32 rounding of the rotation, at most 2^-21 * (|x_i| + |x_{i+D/2}|)
+ * (visible only where the two products cancel).  Supported: D == 64.
+ */
+tvl_status tvl_rope_paged_kv_write(void* q, const void* k_new, const void* v_new,
+                                   void* k_cache, void* v_cache,
+                                   const int32_t* slot_mapping,
+                                   const int32_t* positions, int num_tokens,
+                                   int num_q_heads, int num_kv_heads,
+                                   int head_dim, int block_size, int num_blocks,
+                                   float rope_theta, void* stream);
+
+/*
  * Workspace needed by tvl_paged_attention_decode for these sizes, written to
  * *bytes.  The arguments mean what they mean in the decode call and are
  * validated the same way.  With partition_size == 0 the answer depends on the

@@ -66,6 +66,13 @@ def _load():
             lib.oracle_prefill.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I,
                                            ctypes.c_double, P]
             lib.oracle_prefill.restype = I
+            lib.oracle_rope_double.argtypes = [P, P, I, LL, ctypes.c_double]
+            lib.oracle_rope_double.restype = None
+            lib.oracle_rope_kv_write.argtypes = [P, P, P, P, P, P, P, LL, I, I, I, LL,
+                                                 ctypes.c_double]
+            lib.oracle_rope_kv_write.restype = LL
+            lib.oracle_round_bf16.argtypes = [P, P, LL]
+            lib.oracle_round_bf16.restype = None
             lib.oracle_set_threads.argtypes = [I]
             lib.oracle_set_threads.restype = None
             lib.oracle_max_threads.argtypes = []
@@ -170,4 +177,40 @@ def prefill(q, query_start_loc, k_cache, v_cache, block_tables, context_lens, sc
                                 _ptr(mask) if mask is not None else None)
     if rc != 0:
         raise OracleError(ERRORS.get(int(rc), str(rc)))
+    return out
+
+
+def rope_double(x, pos: int, theta: float) -> np.ndarray:
+    """Rotary embedding of one float64 head vector (no rounding)."""
+    xv = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty_like(xv)
+    _load().oracle_rope_double(_ptr(y), _ptr(xv), xv.shape[0], int(pos), float(theta))
+    return y
+
+
+def rope_kv_write(q, k_cache, v_cache, k_new, v_new, slot_mapping, positions, theta):
+    """Returns (q', k_cache', v_cache') as new uint16 arrays: q and the new K
+    rotated at their positions (rounded to bf16), K/V rows written."""
+    qb = _bits(q).copy() if q is not None else None
+    kc = _bits(k_cache).copy()
+    vc = _bits(v_cache).copy()
+    kn = _bits(k_new)
+    vn = _bits(v_new)
+    sm = _i32(slot_mapping)
+    pos = _i32(positions)
+    nb, bs, hkv, d = kc.shape
+    hq = qb.shape[1] if qb is not None else 0
+    rc = _load().oracle_rope_kv_write(_ptr(qb) if qb is not None else None, _ptr(kc), _ptr(vc),
+                                      _ptr(kn), _ptr(vn), _ptr(sm), _ptr(pos), sm.shape[0], hq,
+                                      hkv, d, nb * bs, float(theta))
+    if rc < 0:
+        raise OracleError(ERRORS.get(int(rc), str(rc)))
+    return qb, kc, vc
+
+
+def round_bf16(values) -> np.ndarray:
+    """float64 values -> bf16 bit patterns (round to nearest, ties to even)."""
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint16)
+    _load().oracle_round_bf16(_ptr(out), _ptr(v), v.size)
     return out

@@ -98,6 +98,99 @@ long long oracle_kv_write(uint16_t* k_cache, uint16_t* v_cache,
   return written;
 }
 
+/*
+ * Rotary position embedding of one head vector, in double precision
+ * [tiny-vllm README, curriculum "RoPE"; Tiny-vLLM digest, "Core Mechanics"]:
+ * for i < D/2 the pair (x_i, x_{i+D/2}) is rotated by the angle
+ * pos * theta^(-2i/D):
+ *   y_i       = x_i cos a - x_{i+D/2} sin a
+ *   y_{i+D/2} = x_{i+D/2} cos a + x_i sin a.
+ */
+void oracle_rope_double(double* y, const double* x, int d, long long pos, double theta) {
+  const int half = d / 2;
+  for (int i = 0; i < half; ++i) {
+    const double inv_freq = pow(theta, -2.0 * i / d);
+    const double a = (double)pos * inv_freq;
+    const double c = cos(a), s = sin(a);
+    y[i] = x[i] * c - x[i + half] * s;
+    y[i + half] = x[i + half] * c + x[i] * s;
+  }
+}
+
+/* double -> bf16 bit pattern, rounded to nearest, ties to even (finite
+ * inputs).  The magnitude is bracketed by its two bf16 neighbours and the
+ * nearer one is taken, so the double is rounded once. */
+static uint16_t double_to_bf16_bits(double v) {
+  const uint32_t sign = v < 0 ? 0x80000000u : 0u;
+  const double a = fabs(v);
+  float f = (float)a;
+  uint32_t lo;
+  memcpy(&lo, &f, 4);
+  lo &= 0xffff0000u;                       /* bf16 at or below f */
+  float flo;
+  memcpy(&flo, &lo, 4);
+  if ((double)flo > a) {                   /* f was rounded up past a */
+    lo -= 0x10000u;
+    memcpy(&flo, &lo, 4);
+  }
+  const uint32_t hi = lo + 0x10000u;
+  float fhi;
+  memcpy(&fhi, &hi, 4);
+  const double dl = a - (double)flo, dh = (double)fhi - a;
+  uint32_t pick;
+  if (dl < dh) pick = lo;
+  else if (dh < dl) pick = hi;
+  else pick = ((lo >> 16) & 1u) ? hi : lo;
+  return (uint16_t)((pick | sign) >> 16);
+}
+
+/* Rounds n doubles to bf16 bit patterns (exported for the rounding pin). */
+void oracle_round_bf16(uint16_t* out, const double* in, long long n) {
+  for (long long i = 0; i < n; ++i) out[i] = double_to_bf16_bits(in[i]);
+}
+
+/*
+ * RoPE + paged KV write: for every token t, q[t] (if q is not NULL) and k_new[t]
+ * are rotated at position positions[t] (each head separately), rounded to
+ * bf16; then, for slot_mapping[t] >= 0, the rotated K row and the V row are
+ * stored at that slot.  q is rotated in place for every token.
+ */
+long long oracle_rope_kv_write(uint16_t* q, uint16_t* k_cache, uint16_t* v_cache,
+                               const uint16_t* k_new, const uint16_t* v_new,
+                               const int32_t* slot_mapping, const int32_t* positions,
+                               long long num_tokens, int hq, int hkv, int d,
+                               long long num_slots, double theta) {
+  if (d <= 0 || d % 2) return -1;
+  double x[512], y[512];
+  if (d > 512) return -1;
+  long long written = 0;
+  for (long long t = 0; t < num_tokens; ++t)
+    if (slot_mapping[t] >= num_slots) return -2;
+  for (long long t = 0; t < num_tokens; ++t) {
+    const long long pos = positions[t];
+    if (q) {
+      for (int h = 0; h < hq; ++h) {
+        uint16_t* row = q + (t * hq + h) * d;
+        for (int e = 0; e < d; ++e) x[e] = bf16_bits_to_double(row[e]);
+        oracle_rope_double(y, x, d, pos, theta);
+        for (int e = 0; e < d; ++e) row[e] = double_to_bf16_bits(y[e]);
+      }
+    }
+    const long long slot = slot_mapping[t];
+    if (slot < 0) continue;
+    for (int h = 0; h < hkv; ++h) {
+      const uint16_t* src = k_new + (t * hkv + h) * d;
+      uint16_t* dst = k_cache + (slot * hkv + h) * d;
+      for (int e = 0; e < d; ++e) x[e] = bf16_bits_to_double(src[e]);
+      oracle_rope_double(y, x, d, pos, theta);
+      for (int e = 0; e < d; ++e) dst[e] = double_to_bf16_bits(y[e]);
+    }
+    memcpy(v_cache + slot * hkv * d, v_new + t * hkv * d, (size_t)hkv * d * sizeof(uint16_t));
+    ++written;
+  }
+  return written;
+}
+
 /* Checks a sequence's context length and the block ids it will read. */
 static int check_sequence(const int32_t* table_row, long long ctx, int bs,
                           int num_blocks, int max_blocks) {

@@ -20,6 +20,7 @@ import torch
 
 __all__ = [
     "TvlError", "paged_kv_write", "paged_attention_decode", "copy_blocks", "BlockAllocator",
+    "rope_paged_kv_write",
     "paged_attention_decode_workspace_size", "paged_attention_prefill", "get_device_status",
     "version", "library_path", "DEV_BAD_SLOT", "DEV_BAD_BLOCK_ID", "DEV_BAD_CONTEXT_LEN",
     "DEV_BAD_QUERY_LEN", "DEV_TIMEOUT",
@@ -77,6 +78,8 @@ def _load():
             lib.tvl_last_error.restype = ctypes.c_char_p
             lib.tvl_version.argtypes = []
             lib.tvl_version.restype = I
+            lib.tvl_rope_paged_kv_write.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, P]
+            lib.tvl_rope_paged_kv_write.restype = I
             lib.tvl_copy_blocks.argtypes = [P, P, P, P, I, I, I, I, I, P]
             lib.tvl_copy_blocks.restype = I
             I32P = ctypes.POINTER(ctypes.c_int32)
@@ -156,6 +159,34 @@ def paged_kv_write(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None) ->
         _check(_load().tvl_paged_kv_write(_ptr(k_new), _ptr(v_new), _ptr(k_cache),
                                           _ptr(v_cache), _ptr(slot_mapping), t, hkv, d, bs, nb,
                                           _stream(stream)))
+
+
+def rope_paged_kv_write(q, k_new, v_new, k_cache, v_cache, slot_mapping, positions,
+                        rope_theta=500000.0, stream=None) -> None:
+    """RoPE of q (in place; may be None) and of k_new at `positions` (int32
+    [T]), then the paged write of the rotated K rows and the V rows."""
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    dev = k_cache.device
+    _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _need(k_new, "k_new", torch.bfloat16, 3, dev)
+    _need(v_new, "v_new", torch.bfloat16, 3, dev)
+    _need(slot_mapping, "slot_mapping", torch.int32, 1, dev)
+    _need(positions, "positions", torch.int32, 1, dev)
+    nb, bs, hkv, d = k_cache.shape
+    t = slot_mapping.shape[0]
+    hq = 0
+    if q is not None:
+        _need(q, "q", torch.bfloat16, 3, dev)
+        if q.shape[0] != t or q.shape[2] != d:
+            raise ValueError("q must be [T, Hq, D]")
+        hq = q.shape[1]
+    if k_new.shape != (t, hkv, d) or v_new.shape != (t, hkv, d) or positions.shape[0] != t:
+        raise ValueError("k_new/v_new must be [T, Hkv, D] and positions [T]")
+    with torch.cuda.device(dev):
+        _check(_load().tvl_rope_paged_kv_write(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                               _ptr(v_cache), _ptr(slot_mapping),
+                                               _ptr(positions), t, hq, hkv, d, bs, nb,
+                                               float(rope_theta), _stream(stream)))
 
 
 def paged_attention_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,

@@ -202,6 +202,47 @@ tvl_status tvl_paged_kv_write(const void* k_new, const void* v_new, void* k_cach
   return TVL_OK;
 }
 
+tvl_status tvl_rope_paged_kv_write(void* q, const void* k_new, const void* v_new, void* k_cache,
+                                   void* v_cache, const int32_t* slot_mapping,
+                                   const int32_t* positions, int num_tokens, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                   float rope_theta, void* stream) {
+  if (num_tokens < 0) return fail(TVL_ERR_INVALID_ARG, "num_tokens %d < 0", num_tokens);
+  if (num_kv_heads <= 0 || block_size <= 0 || num_blocks <= 0 || num_q_heads < 0)
+    return fail(TVL_ERR_INVALID_ARG, "head counts, block_size and num_blocks must be positive");
+  if (head_dim != 64) return fail(TVL_ERR_UNSUPPORTED, "head_dim %d (supported: 64)", head_dim);
+  if (!(rope_theta > 1.0f) || !std::isfinite(rope_theta))
+    return fail(TVL_ERR_INVALID_ARG, "rope_theta must be finite and > 1");
+  if (!k_cache || !v_cache) return fail(TVL_ERR_INVALID_ARG, "null cache pointer");
+  if (!aligned16(k_cache) || !aligned16(v_cache))
+    return fail(TVL_ERR_INVALID_ARG, "cache pointers must be 16-byte aligned");
+  if (num_tokens == 0) return TVL_OK;
+  if (!k_new || !v_new || !slot_mapping || !positions)
+    return fail(TVL_ERR_INVALID_ARG, "null input pointer");
+  if (q && num_q_heads == 0) return fail(TVL_ERR_INVALID_ARG, "q given with no query heads");
+  if (!aligned16(v_new)) return fail(TVL_ERR_INVALID_ARG, "v_new must be 16-byte aligned");
+  uint32_t* word = nullptr;
+  tvl_status st = status_word(&word);
+  if (st != TVL_OK) return st;
+  tvl::RopeKvWriteArgs a;
+  a.q = q;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.slot_mapping = slot_mapping;
+  a.positions = positions;
+  a.num_tokens = num_tokens;
+  a.num_q_heads = q ? num_q_heads : 0;
+  a.num_kv_heads = num_kv_heads;
+  a.num_slots = static_cast<long long>(num_blocks) * block_size;
+  a.log2_theta = std::log2(static_cast<double>(rope_theta));
+  a.status = word;
+  cudaError_t e = tvl::launch_rope_kv_write(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rope_kv_write launch");
+  return TVL_OK;
+}
+
 tvl_status tvl_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst,
                            int n, int num_kv_heads, int head_dim, int block_size, int num_blocks,
                            void* stream) {

@@ -21,6 +21,21 @@ struct KvWriteArgs {
 };
 cudaError_t launch_kv_write(const KvWriteArgs& a, cudaStream_t stream);
 
+struct RopeKvWriteArgs {
+  void* q;                 // may be null
+  const void* k_new;
+  const void* v_new;
+  void* k_cache;
+  void* v_cache;
+  const int32_t* slot_mapping;
+  const int32_t* positions;
+  int num_tokens, num_q_heads, num_kv_heads;
+  long long num_slots;
+  double log2_theta;
+  uint32_t* status;
+};
+cudaError_t launch_rope_kv_write(const RopeKvWriteArgs& a, cudaStream_t stream);
+
 struct CopyBlocksArgs {
   void* k_cache;
   void* v_cache;

@@ -326,16 +326,26 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
       for (int c = 0; c < 2; ++c) {
         uint32_t ph[16];
 #pragma unroll
+        if (masked) {
+#pragma unroll
         for (int e = 0; e < 32; e += 2) {
           float2 x = make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
           x = __ffma2_rn(x, sl2, nm2);
-          if (masked) {
-            if (col0 + c * 32 + e > limit) x.x = -INFINITY;
-            if (col0 + c * 32 + e + 1 > limit) x.y = -INFINITY;
-          }
+          if (col0 + c * 32 + e > limit) x.x = -INFINITY;
+          if (col0 + c * 32 + e + 1 > limit) x.y = -INFINITY;
           const float2 pv = make_float2(ex2(x.x), ex2(x.y));
           sum = __fadd2_rn(sum, pv);
           ph[e / 2] = pack_half2(pv.x, pv.y);
+        }
+        } else {
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float2 x = make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+          x = __ffma2_rn(x, sl2, nm2);
+          const float2 pv = make_float2(ex2(x.x), ex2(x.y));
+          sum = __fadd2_rn(sum, pv);
+          ph[e / 2] = pack_half2(pv.x, pv.y);
+        }
         }
         tmem_st16(p_addr + col0 / 2 + c * 16, ph);
       }
