@@ -12,25 +12,27 @@
 // (NH = 2 when the group has two or more heads), so each K/V tile gathered
 // from the paged cache serves NH heads.  Warps:
 //   0..4NH-1  softmax, one warpgroup per head: thread r owns query row r
-//             (TMEM lane r).  Per 128-key tile it converts its share of the V
-//             tile bf16 -> fp16 in place (exact for |v| >= 2^-14; keys past
-//             the context become 0) while its S loads are in flight, then
-//             computes P = 2^(S*scale*log2e - m) with packed fp32x2 arithmetic
-//             against a running reference maximum m and stores it as fp16
-//             into TMEM.  m is set by the first tile and moved only on masked
-//             (diagonal / context-tail) tiles or when a tile's row sum shows
-//             that some P could overflow fp16; O in TMEM is rescaled when it
-//             moves (exact: one reference maximum scales numerator and
-//             denominator).  At the end it normalises O and writes it out;
+//             (TMEM lane r).  Per 128-key tile it loads its 128 scores into
+//             registers, converting its share of the V tile bf16 -> fp16 in
+//             place while the loads fly (exact for |v| >= 2^-14; keys past
+//             the context become 0), and releases S at once so the next
+//             tile's Q K^T overlaps the rest.  It then computes
+//             P = 2^(S*scale*log2e - m) with packed fp32x2 arithmetic against
+//             a reference maximum m that moves only when a tile's maximum
+//             exceeds it by more than 2^8 (O in TMEM is then rescaled; exact,
+//             since one reference scales numerator and denominator), and
+//             stores P as fp16 into TMEM once the previous P.V has consumed
+//             the buffer.  At the end it normalises O and writes it out;
 //   4NH       producer: TMA loads of the Q tiles and, per 128-key tile, one
 //             box of bs tokens x 64 dims per physical block (K and V) found
 //             through the block table -- the paged gather; blocks past the
 //             context are requested out of range, so TMA fills them with 0;
 //   4NH+1     MMA issuer: S_h = Q_h K^T (M 128, N 128, bf16, both operands in
 //             shared memory) and O_h += P_h V (M 128, N 64, fp16, P read from
-//             TMEM, V an MN-major shared operand), fp32 accumulation; the
-//             heads' MMAs alternate so one head's softmax overlaps the other
-//             head's tensor work.  Completion is signalled by tcgen05.commit.
+//             TMEM, V an MN-major shared operand), fp32 accumulation.  The
+//             next tile's S is issued as soon as the softmax has released S,
+//             before this tile's P.V, so the tensor pipe works while P is
+//             computed.  Completion is signalled by tcgen05.commit.
 // P and V go through fp16 rather than bf16 so that rounding P costs at most
 // 2^-11 relative (bf16 would cost 2^-8) -- the fp32-accumulated result stays
 // within 2e-3 of the exact attention even for rows with few keys.
@@ -84,6 +86,7 @@ struct Barriers {
   uint64_t kv_empty[kStages];
   uint64_t v_ready[kStages];
   uint64_t s_full[2];
+  uint64_t s_free[2];
   uint64_t p_full[2];
   uint64_t pv_done[2];
   uint64_t mma_done;
@@ -190,6 +193,7 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
     }
     for (int i = 0; i < NH; ++i) {
       mbar_init(&B->s_full[i], 1);
+      mbar_init(&B->s_free[i], 4);
       mbar_init(&B->p_full[i], 4);
       mbar_init(&B->pv_done[i], 1);
     }
@@ -252,6 +256,10 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
     }
   } else if (warp == C::kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
+    // Per key tile j and head h: S_h(j+1) = Q_h K(j+1)^T is issued as soon as
+    // the softmax has taken S_h(j) into registers (s_free), so it runs while
+    // P_h(j) is being computed; O_h += P_h(j) V(j) follows once P_h(j) is in
+    // TMEM (p_full) and V(j) is fp16 (v_ready).
     if (lane == 0) {
       const uint32_t q_addr = smem_addr(smem + C::kQOff);
       auto issue_qk = [&](int j, int hh) {
@@ -270,6 +278,15 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
       }
       for (int j = 0; ok && j < n_kv; ++j) {
         const int st = j % kStages;
+        if (j + 1 < n_kv) {
+          ok = wait_or_abort(&B->kv_full[(j + 1) % kStages], ((j + 1) / kStages) & 1, B, p);
+          for (int hh = 0; ok && hh < NH; ++hh) {
+            ok = wait_or_abort(&B->s_free[hh], j & 1, B, p);
+            if (!ok) break;
+            tc_fence_after();
+            issue_qk(j + 1, hh);
+          }
+        }
         for (int hh = 0; ok && hh < NH; ++hh) {
           ok = wait_or_abort(&B->p_full[hh], j & 1, B, p) &&
                wait_or_abort(&B->v_ready[st], (j / kStages) & 1, B, p);
@@ -282,13 +299,6 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
                        desc_sw128(v_addr + kk * 2048, 16, 1024), kIdescPV, (j > 0 || kk > 0));
           mma_commit(&B->pv_done[hh]);
           if (hh == NH - 1) mma_commit(&B->kv_empty[st]);
-          if (j + 1 < n_kv) {
-            if (hh == 0) ok = wait_or_abort(&B->kv_full[(j + 1) % kStages],
-                                            ((j + 1) / kStages) & 1, B, p);
-            if (!ok) break;
-            tc_fence_after();
-            issue_qk(j + 1, hh);
-          }
         }
       }
       // every MMA issued must be complete before TMEM is released
@@ -311,76 +321,9 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
     const int vchunk0 = NH == 2 ? (r & 1) * 4 : 0;
     const int vchunks = NH == 2 ? 4 : 8;
     const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
-    (void)kRescaleLog2;
-    float m_used = -INFINITY;
+    float m_used = -INFINITY;                           // reference maximum (log2 units)
     float2 l2 = make_float2(0.f, 0.f);
     bool ok = true;
-    // P for 64 columns [col0, col0 + 64) of this row from scores already in
-    // registers: p = 2^(s * scale * log2e - m), fp16 pairs into TMEM columns
-    // P + col0 / 2; returns the sum of the p (fp32, before rounding).
-    auto emit_p = [&](const uint32_t (&sr)[2][32], int col0, float mref, bool masked,
-                      int limit) -> float2 {
-      const float2 nm2 = make_float2(-mref, -mref);
-      float2 sum = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t ph[16];
-#pragma unroll
-        if (masked) {
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float2 x = make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-          x = __ffma2_rn(x, sl2, nm2);
-          if (col0 + c * 32 + e > limit) x.x = -INFINITY;
-          if (col0 + c * 32 + e + 1 > limit) x.y = -INFINITY;
-          const float2 pv = make_float2(ex2(x.x), ex2(x.y));
-          sum = __fadd2_rn(sum, pv);
-          ph[e / 2] = pack_half2(pv.x, pv.y);
-        }
-        } else {
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float2 x = make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-          x = __ffma2_rn(x, sl2, nm2);
-          const float2 pv = make_float2(ex2(x.x), ex2(x.y));
-          sum = __fadd2_rn(sum, pv);
-          ph[e / 2] = pack_half2(pv.x, pv.y);
-        }
-        }
-        tmem_st16(p_addr + col0 / 2 + c * 16, ph);
-      }
-      return sum;
-    };
-    // maximum of the scaled, masked scores of 64 columns in registers
-    auto tile_max = [&](const uint32_t (&sr)[2][32], int col0, bool masked, int limit) {
-      float mt = -INFINITY;
-      if (masked) {
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float v = __uint_as_float(sr[c][e]) * p.scale_log2;
-            if (col0 + c * 32 + e > limit) v = -INFINITY;
-            mt = fmaxf(mt, v);
-          }
-      } else if (p.scale_log2 >= 0.f) {
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            mt = max3(mt, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-        mt *= p.scale_log2;
-      } else {
-        float mn = INFINITY;
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            mn = min3(mn, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-        mt = mn * p.scale_log2;
-      }
-      return mt;
-    };
 
     for (int j = 0; j < n_kv && ok; ++j) {
       const int st = j % kStages;
@@ -389,9 +332,9 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
            wait_or_abort(&B->s_full[hh], j & 1, B, p);
       if (__any_sync(kFull, !ok)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sa[2][32];                               // columns [0, 64)
-      tmem_ld32(s_addr, sa[0]);
-      tmem_ld32(s_addr + 32, sa[1]);
+      uint32_t sr[4][32];                               // this row's 128 scores
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
       // --- while those loads fly: V tile j bf16 -> fp16 in place (keys past
       // the context -> 0), this warpgroup's share of the rows
       {
@@ -417,79 +360,104 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
         if (lane == 0) mbar_arrive(&B->v_ready[st]);
       }
       tmem_ld_wait();
+      // S_h is in registers: the next tile's Q K^T may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B->s_free[hh]);
 
-      // Tiles on the causal diagonal or past the context need the mask, and
-      // the first tile sets the running maximum: those take the exact path.
-      // Every other tile computes P against the running maximum directly and
-      // only falls back to the exact path if its row sum exceeds 60000: below
-      // that every P fits fp16 (max 65504), and the result is exact either
-      // way because one reference maximum scales numerator and denominator.
+      // Tiles on the causal diagonal or past the context need the mask.
       const bool masked = (key0 + kBN - 1 > pos_first) || (key0 + kBN > ctx);
       const int limit = min(qpos, ctx - 1) - key0;     // last visible column
-      bool exact = masked || j == 0;
+      // row maximum of the scaled scores of this tile
+      float mt;
+      if (masked) {
+        mt = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float v = __uint_as_float(sr[c][e]) * p.scale_log2;
+            if (c * 32 + e > limit) v = -INFINITY;
+            mt = fmaxf(mt, v);
+          }
+      } else if (p.scale_log2 >= 0.f) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            mx = max3(mx, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+        mt = mx * p.scale_log2;
+      } else {
+        float mn = INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            mn = min3(mn, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+        mt = mn * p.scale_log2;
+      }
+      // The reference maximum moves only when the tile's maximum exceeds it
+      // by more than 2^8, so every P <= 256 fits fp16; the result is exact
+      // either way because one reference scales numerator and denominator.
+      float f = 1.f;
+      const bool move = j == 0 ? true : mt > m_used + kRescaleLog2;
+      if (move) {
+        f = j == 0 ? 1.f : ex2(m_used - mt);
+        m_used = mt;
+      }
+      const float mref = m_used == -INFINITY ? 0.f : m_used;
+      const float2 nm2 = make_float2(-mref, -mref);
+      // P = 2^(s * scale * log2e - m) in registers, fp16 pairs
+      uint32_t pk[2][32];
       float2 tsum = make_float2(0.f, 0.f);
-      if (!exact) {
-        // P_h of tile j-1 must have been consumed before it is overwritten
+      if (masked) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float2 x = make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+            x = __ffma2_rn(x, sl2, nm2);
+            if (c * 32 + e > limit) x.x = -INFINITY;
+            if (c * 32 + e + 1 > limit) x.y = -INFINITY;
+            const float2 pv = make_float2(ex2(x.x), ex2(x.y));
+            tsum = __fadd2_rn(tsum, pv);
+            pk[c >> 1][(c & 1) * 16 + e / 2] = pack_half2(pv.x, pv.y);
+          }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float2 x = make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+            x = __ffma2_rn(x, sl2, nm2);
+            const float2 pv = make_float2(ex2(x.x), ex2(x.y));
+            tsum = __fadd2_rn(tsum, pv);
+            pk[c >> 1][(c & 1) * 16 + e / 2] = pack_half2(pv.x, pv.y);
+          }
+      }
+      // P_h(j-1) must have been consumed (and O_h(j-1) complete) before P_h
+      // is overwritten and O_h rescaled
+      if (j > 0) {
         ok = wait_or_abort(&B->pv_done[hh], (j - 1) & 1, B, p);
         if (__any_sync(kFull, !ok)) { ok = false; break; }
         tc_fence_after();
-        tsum = emit_p(sa, 0, m_used, false, 0);
-        uint32_t sb[2][32];
-        tmem_ld32(s_addr + 64, sb[0]);
-        tmem_ld32(s_addr + 96, sb[1]);
-        tmem_ld_wait();
-        tsum = __fadd2_rn(tsum, emit_p(sb, 64, m_used, false, 0));
-        exact = __any_sync(kFull, tsum.x + tsum.y > 60000.f);   // < fp16 max 65504
-        if (exact) {
-          tmem_ld32(s_addr, sa[0]);
-          tmem_ld32(s_addr + 32, sa[1]);
-          tmem_ld_wait();
-        }
-      }
-      if (exact) {
-        // one half of the scores in registers at a time
-        const float ma = tile_max(sa, 0, masked, limit);
-        uint32_t sb[2][32];
-        tmem_ld32(s_addr + 64, sb[0]);
-        tmem_ld32(s_addr + 96, sb[1]);
-        tmem_ld_wait();
-        const float mt = fmaxf(ma, tile_max(sb, 64, masked, limit));
-        const float m_new = fmaxf(m_used, mt);
-        const bool need = m_new > m_used;
-        if (j > 0) {
-          // O *= f (when the maximum moved) and the P buffer reuse both need
-          // the previous P.V to have landed
-          ok = wait_or_abort(&B->pv_done[hh], (j - 1) & 1, B, p);
-          if (__any_sync(kFull, !ok)) { ok = false; break; }
-          tc_fence_after();
-        }
-        if (__any_sync(kFull, need)) {
-          const float f = need ? ex2(m_used - m_new) : 1.0f;
-          if (j > 0) {
+        if (__any_sync(kFull, move)) {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              uint32_t o[32];
-              tmem_ld32(o_addr + c * 32, o);
-              tmem_ld_wait();
+          for (int c = 0; c < 2; ++c) {
+            uint32_t o[32];
+            tmem_ld32(o_addr + c * 32, o);
+            tmem_ld_wait();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-              tmem_st32(o_addr + c * 32, o);
-            }
-          }
-          if (need) {
-            m_used = m_new;
-            l2.x *= f;
-            l2.y *= f;
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+            tmem_st32(o_addr + c * 32, o);
           }
         }
-        const float mref = m_used == -INFINITY ? 0.f : m_used;
-        tsum = emit_p(sb, 64, mref, masked, limit);
-        tmem_ld32(s_addr, sa[0]);
-        tmem_ld32(s_addr + 32, sa[1]);
-        tmem_ld_wait();
-        tsum = __fadd2_rn(tsum, emit_p(sa, 0, mref, masked, limit));
       }
-      l2 = __fadd2_rn(l2, tsum);
+      l2.x = fmaf(l2.x, f, tsum.x);
+      l2.y = fmaf(l2.y, f, tsum.y);
+      tmem_st32(p_addr, pk[0]);
+      tmem_st32(p_addr + 32, pk[1]);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
