@@ -387,7 +387,8 @@ def prefill_line(wl, args, r, bf16_sus, peak_src):
                    "l2": f"{r['copies']} rotating copies of q and the caches"},
         "roofline": {"kernel": "prefill_kernel", "bound": "tensor", "achieved": round(achieved, 1),
                      "peak": bf16_sus, "unit": "TFLOP/s", "frac": round(achieved / bf16_sus, 4),
-                     "traffic": None,
+                     "traffic": recorded_traffic("prefill_chunked_prefill.txt",
+                                                 ["prefill.cu", "tc.cuh", "device.cuh"]),
                      "peak_source": f"{peak_src} bf16_tflops_sustained (the kernel runs in a "
                                     f"seconds-long loop)",
                      "launch_ms_mean": round(r["kernel_ms"], 5),

@@ -196,3 +196,35 @@ def test_decode_workspace_too_small_is_rejected():
         tvl.paged_attention_decode(out, t["q"], t["k_cache"], t["v_cache"], t["block_tables"],
                                    t["context_lens"], wl.scale, partition_size=0, workspace=ws)
     assert ei.value.status == tvl.ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("part", [0, 256])
+def test_decode_ignores_workspace_contents(part):
+    """The split-K tickets in the workspace are tagged per call, so a
+    workspace full of arbitrary bytes gives the same result as a zeroed one,
+    and reusing it for a second call changes nothing."""
+    wl = W.make_decode(77, [5000, 17, 3000, 1, 700, 4096], num_q_heads=32, num_kv_heads=8,
+                       block_size=16)
+    t = W.to_device(wl, DEV)
+    s, hq, d = wl.q.shape
+    size = tvl.paged_attention_decode_workspace_size(s, hq, wl.num_kv_heads, d,
+                                                     wl.max_blocks_per_seq, wl.block_size, part)
+    assert size > 0
+    outs = []
+    for fill in ("zeros", "random", "random"):
+        if fill == "zeros":
+            ws = torch.zeros(size, dtype=torch.uint8, device=DEV)
+        else:
+            ws = torch.randint(0, 256, (size,), dtype=torch.uint8, device=DEV)
+        for _ in range(2):
+            out = torch.empty(s, hq, d, dtype=torch.float32, device=DEV)
+            tvl.paged_attention_decode(out, t["q"], t["k_cache"], t["v_cache"], t["block_tables"],
+                                       t["context_lens"], wl.scale, partition_size=part,
+                                       workspace=ws)
+            torch.cuda.synchronize()
+            outs.append(out.cpu())
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    ref = oracle.decode(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale)
+    assert_close(outs[0].double().numpy(), ref, "decode")
+    assert_clean_status()
