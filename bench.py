@@ -206,15 +206,14 @@ def bench_decode(wl, args, rank, world, device):
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
 
-    def step(t, ev=None):
-        tvl.paged_kv_write(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["slot_mapping"])
-        if ev is not None:
-            ev[0].record(stream)
-        tvl.paged_attention_decode(out, t["q"], t["k_cache"], t["v_cache"], t["block_tables"],
-                                   t["context_lens"], wl.scale, partition_size=part,
-                                   workspace=ws)
-        if ev is not None:
-            ev[1].record(stream)
+    if wl.k_new.shape[0] != s:
+        raise SystemExit("the decode step needs a new token for every sequence")
+
+    def step(t):
+        # one call: the new tokens' paged write fused into the decode (+ merge)
+        tvl.paged_decode_step(out, t["q"], t["k_new"], t["v_new"], t["k_cache"], t["v_cache"],
+                              t["block_tables"], t["context_lens"], wl.scale,
+                              partition_size=part, workspace=ws)
 
     for i in range(args.warmup):
         step(sets[i % copies])
@@ -222,8 +221,9 @@ def bench_decode(wl, args, rank, world, device):
     if tvl.get_device_status() != 0:
         raise RuntimeError("device status word set during warm-up")
 
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+    # The timed steps run back to back (each step is one call, so its average
+    # duration is the call's); no event sits between the calls, which would
+    # break the programmatic overlap of one call's launch with the previous.
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
     if world > 1:
@@ -237,7 +237,7 @@ def bench_decode(wl, args, rank, world, device):
         host_t0 = time.time()
         start.record(stream)
         for i in range(args.steps):
-            step(sets[i % copies], evs[i])
+            step(sets[i % copies])
         stop.record(stream)
         torch.cuda.synchronize(device)
         host_t1 = time.time()
@@ -245,13 +245,12 @@ def bench_decode(wl, args, rank, world, device):
     if world > 1:
         torch.distributed.barrier()
     elapsed_ms = start.elapsed_time(stop)
-    dec_ms = [a.elapsed_time(b) for a, b in evs]
 
     # end to end through the public API: H2D of the step's inputs from pinned
     # host memory, the two calls, D2H of the output
     host = {k: v.pin_memory() for k, v in
-            W.to_device(wl, "cpu").items() if k in ("q", "k_new", "v_new", "slot_mapping",
-                                                     "block_tables", "context_lens")}
+            W.to_device(wl, "cpu").items() if k in ("q", "k_new", "v_new", "block_tables",
+                                                     "context_lens")}
     out_host = torch.empty(s, hq, d, dtype=torch.float32).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = out_host.numel() * out_host.element_size()
@@ -260,11 +259,9 @@ def bench_decode(wl, args, rank, world, device):
     def e2e_step(t):
         for k, v in host.items():
             dev_in[k].copy_(v, non_blocking=True)
-        tvl.paged_kv_write(dev_in["k_new"], dev_in["v_new"], t["k_cache"], t["v_cache"],
-                           dev_in["slot_mapping"])
-        tvl.paged_attention_decode(out, dev_in["q"], t["k_cache"], t["v_cache"],
-                                   dev_in["block_tables"], dev_in["context_lens"], wl.scale,
-                                   partition_size=part, workspace=ws)
+        tvl.paged_decode_step(out, dev_in["q"], dev_in["k_new"], dev_in["v_new"], t["k_cache"],
+                              t["v_cache"], dev_in["block_tables"], dev_in["context_lens"],
+                              wl.scale, partition_size=part, workspace=ws)
         out_host.copy_(out, non_blocking=True)
 
     for i in range(args.warmup):
@@ -281,11 +278,10 @@ def bench_decode(wl, args, rank, world, device):
     if tvl.get_device_status() != 0:
         raise RuntimeError("device status word set during timing")
     return {
-        "elapsed_ms": elapsed_ms, "decode_ms": statistics.mean(dec_ms),
-        "decode_ms_median": statistics.median(dec_ms), "e2e_ms": e2e_ms,
+        "elapsed_ms": elapsed_ms, "decode_ms": elapsed_ms / args.steps, "e2e_ms": e2e_ms,
         "h2d": h2d, "d2h": d2h, "copies": copies, "clocks": clocks.summary(host_t0, host_t1),
-        "launches_per_step": 3 if (part == 0 or wl.max_blocks_per_seq * wl.block_size > part)
-        else 2,
+        "launches_per_step": 2 if (part == 0 or wl.max_blocks_per_seq * wl.block_size > part)
+        else 1,
     }
 
 
@@ -301,30 +297,35 @@ def bench_prefill(wl, args, device):
     out = torch.empty(tuple(wl.q.shape), dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
 
-    def step(t, ev=None):
-        tvl.paged_kv_write(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["slot_mapping"])
-        if ev is not None:
-            ev[0].record(stream)
+    def prefill(t):
         tvl.paged_attention_prefill(out, t["q"], t["query_start_loc"], t["k_cache"],
                                     t["v_cache"], t["block_tables"], t["context_lens"], wl.scale,
                                     wl.max_q_len)
-        if ev is not None:
-            ev[1].record(stream)
 
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+    def step(t):
+        tvl.paged_kv_write(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["slot_mapping"])
+        prefill(t)
+
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
+    k0 = torch.cuda.Event(enable_timing=True)
+    k1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(device.index if device.index is not None else 0) as clocks:
         time.sleep(0.5)
         for i in range(args.warmup):
             step(sets[i % copies])
         torch.cuda.synchronize(device)
         host_t0 = time.time()
+        # the step (write + prefill), back to back
         start.record(stream)
         for i in range(args.steps):
-            step(sets[i % copies], evs[i])
+            step(sets[i % copies])
         stop.record(stream)
+        # the prefill kernel alone, back to back, for its roofline
+        k0.record(stream)
+        for i in range(args.steps):
+            prefill(sets[i % copies])
+        k1.record(stream)
         torch.cuda.synchronize(device)
         host_t1 = time.time()
         time.sleep(0.1)
@@ -359,8 +360,7 @@ def bench_prefill(wl, args, device):
     torch.cuda.synchronize(device)
     return {
         "elapsed_ms": start.elapsed_time(stop),
-        "kernel_ms": statistics.mean(a.elapsed_time(b) for a, b in evs),
-        "kernel_ms_median": statistics.median(a.elapsed_time(b) for a, b in evs),
+        "kernel_ms": k0.elapsed_time(k1) / args.steps,
         "e2e_ms_per_step": e0.elapsed_time(e1) / e2e_steps,
         "h2d": sum(v.numel() * v.element_size() for v in host.values()),
         "d2h": out_host.numel() * out_host.element_size(), "copies": copies,
@@ -392,11 +392,12 @@ def prefill_line(wl, args, r, bf16_sus, peak_src):
                      "peak_source": f"{peak_src} bf16_tflops_sustained (the kernel runs in a "
                                     f"seconds-long loop)",
                      "launch_ms_mean": round(r["kernel_ms"], 5),
-                     "launch_ms_median": round(r["kernel_ms_median"], 5)},
+                     "launch_timing": "prefill calls back to back over a timed region of "
+                                      "their own, CUDA events around it"},
         "e2e": {"value": round(flops / (r["e2e_ms_per_step"] / 1e3) / 1e12, 2),
                 "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"]},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 3 * args.steps,
         "clocks": r["clocks"],
     }
 
@@ -419,12 +420,17 @@ def cpu_baseline_decode(wl, budget_s=10.0):
     return per_step, cores, reps
 
 
+ARM_PARTS = {"0xd4f": "Arm Neoverse V2", "0xd40": "Arm Neoverse V1", "0xd0c": "Arm Neoverse N1",
+             "0xd8e": "Arm Neoverse N3", "0xd84": "Arm Neoverse V3"}
+
+
 def cpu_model():
     try:
         with open("/proc/cpuinfo") as fh:
             for line in fh:
                 if line.lower().startswith(("model name", "cpu part")):
-                    return line.split(":", 1)[1].strip()
+                    v = line.split(":", 1)[1].strip()
+                    return f"{ARM_PARTS[v]} ({v})" if v in ARM_PARTS else v
     except Exception:
         pass
     return os.uname().machine
@@ -522,7 +528,7 @@ def main():
     value = total_bytes * args.steps / (t_ms / 1e3) / 1e9
     e2e_val = total_bytes * args.steps / (e2e_ms / 1e3) / 1e9
 
-    dec_bytes = decode_algorithmic_bytes(wl)
+    dec_bytes = step_bytes            # the call writes the new tokens and decodes
     achieved = dec_bytes / (r["decode_ms"] / 1e3) / 1e9
     traffic = recorded_traffic("decode_llama1b_decode.txt", ["decode.cu", "device.cuh"])
     line = {
@@ -537,20 +543,22 @@ def main():
             "block_size": wl.block_size, "num_blocks": wl.num_blocks,
             "context_tokens": int(wl.context_lens.sum()),
             "partition_size": wl.partition_size,
-            "step": "paged KV write of the new tokens + paged decode (+ split-K merge)",
+            "step": "one tvl_paged_decode_step call: paged KV write of the new tokens fused "
+                    "into the paged decode (+ split-K merge)",
             "bytes_per_step": step_bytes,
             "l2": f"inputs larger than L2: {r['copies']} rotating cache copies, "
                   f"{wl.kv_bytes() / 1e6:.0f} MB K/V read per step vs 129 MB L2",
         },
         "roofline": {
-            "kernel": "decode (decode_kernel + merge_kernel, one C-ABI call)",
+            "kernel": "decode step (decode_kernel with the fused write + merge_kernel, one "
+                      "C-ABI call)",
             "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
             "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
             "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
             else "fallback 6.8 TB/s",
             "algorithmic_bytes_per_launch": dec_bytes,
             "launch_ms_mean": round(r["decode_ms"], 5),
-            "launch_ms_median": round(r["decode_ms_median"], 5),
+            "launch_timing": "calls back to back over the timed region, CUDA events around it",
         },
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"], "ms_per_step": round(e2e_ms / args.steps, 4)},

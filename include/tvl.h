@@ -168,6 +168,34 @@ tvl_status tvl_paged_attention_decode(
     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * One decode step in a single call [tiny-vllm README, curriculum "Why KV
+ * cache exists", "Paged KV cache", "Paged Attention"; nano-vLLM guide ch. 4
+ * "PagedAttention", ch. 5 "The Scheduler" (each step appends one token per
+ * running sequence and attends over its cache)]: for every sequence s with
+ * context_lens[s] >= 1, the new token's K and V rows (k_new[s], v_new[s],
+ * bf16 [S, Hkv, D], device, read) are written into the cache at position
+ * context_lens[s] - 1, i.e. slot block_tables[s][(ctx - 1) / bs] * bs +
+ * (ctx - 1) % bs -- the slot a slot_mapping of this step holds -- and then
+ * the decode of tvl_paged_attention_decode runs over the updated cache.
+ * Same results as tvl_paged_kv_write with that slot_mapping followed by
+ * tvl_paged_attention_decode (the cache bit for bit, the output to the same
+ * bits), with one kernel boundary less: the CTA that streams a sequence's
+ * last block writes the row before it copies the block.
+ * All other arguments, layouts, the workspace and the errors are those of
+ * tvl_paged_attention_decode; k_new and v_new must be 16-byte aligned.  A
+ * sequence with context_lens[s] == 0 writes nothing.  A block-table entry
+ * that is out of range is reported (TVL_DEV_BAD_BLOCK_ID) and its row is not
+ * written.
+ */
+tvl_status tvl_paged_decode_step(
+    float* out, const void* q, const void* k_new, const void* v_new,
+    void* k_cache, void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int block_size, int num_blocks,
+    int max_blocks_per_seq, float scale, int partition_size, void* workspace,
+    size_t workspace_bytes, void* stream);
+
+/*
  * Chunked causal prefill over a cached prefix [tiny-vllm README, curriculum
  * "Prefill vs decode", "Attention", "GQA", "Causal mask", "Online softmax",
  * "Paged Attention"; nano-vLLM guide ch. 6 "Prefill vs Decode", ch. 7

@@ -67,10 +67,12 @@ def _load():
                 P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, SZ, P]
             lib.tvl_paged_attention_prefill.argtypes = [
                 P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P]
+            lib.tvl_paged_decode_step.argtypes = [
+                P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, SZ, P]
             lib.tvl_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
             for name in ("tvl_paged_kv_write", "tvl_paged_attention_decode_workspace_size",
                          "tvl_paged_attention_decode", "tvl_paged_attention_prefill",
-                         "tvl_get_device_status"):
+                         "tvl_paged_decode_step", "tvl_get_device_status"):
                 getattr(lib, name).restype = I
             lib.tvl_status_string.argtypes = [I]
             lib.tvl_status_string.restype = ctypes.c_char_p
@@ -228,6 +230,44 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
             _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
             _ptr(context_lens), s, hq, hkv, d, bs, nb, mb, float(scale), int(partition_size),
             _ptr(workspace), ws_bytes, _stream(stream)))
+    return out
+
+
+def paged_decode_step(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale,
+                      partition_size=0, workspace=None, stream=None):
+    """One decode step (tvl_paged_decode_step): writes k_new / v_new bf16
+    [S, Hkv, D] at position context_lens[s] - 1 of each sequence, then
+    out fp32 [S, Hq, D] <- paged decode attention of q bf16 [S, Hq, D] over
+    the updated cache."""
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    dev = k_cache.device
+    _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _need(q, "q", torch.bfloat16, 3, dev)
+    _need(k_new, "k_new", torch.bfloat16, 3, dev)
+    _need(v_new, "v_new", torch.bfloat16, 3, dev)
+    _need(out, "out", torch.float32, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    nb, bs, hkv, d = k_cache.shape
+    s, hq, d2 = q.shape
+    if d2 != d or out.shape != q.shape or v_cache.shape != k_cache.shape:
+        raise ValueError("inconsistent q / out / cache shapes")
+    if tuple(k_new.shape) != (s, hkv, d) or v_new.shape != k_new.shape:
+        raise ValueError("k_new / v_new must be [num_seqs, num_kv_heads, head_dim]")
+    if block_tables.shape[0] != s or context_lens.shape[0] != s:
+        raise ValueError("block_tables / context_lens must have num_seqs rows")
+    mb = block_tables.shape[1]
+    with torch.cuda.device(dev):
+        need = paged_attention_decode_workspace_size(s, hq, hkv, d, mb, bs, partition_size)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        if workspace is not None:
+            _need(workspace, "workspace", torch.uint8, 1, dev)
+        ws_bytes = workspace.numel() if workspace is not None else 0
+        _check(_load().tvl_paged_decode_step(
+            _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+            _ptr(block_tables), _ptr(context_lens), s, hq, hkv, d, bs, nb, mb, float(scale),
+            int(partition_size), _ptr(workspace), ws_bytes, _stream(stream)))
     return out
 
 

@@ -285,13 +285,14 @@ tvl_status tvl_paged_attention_decode_workspace_size(int num_seqs, int num_q_hea
   return TVL_OK;
 }
 
-tvl_status tvl_paged_attention_decode(float* out, const void* q, const void* k_cache,
-                                      const void* v_cache, const int32_t* block_tables,
-                                      const int32_t* context_lens, int num_seqs, int num_q_heads,
-                                      int num_kv_heads, int head_dim, int block_size,
-                                      int num_blocks, int max_blocks_per_seq, float scale,
-                                      int partition_size, void* workspace, size_t workspace_bytes,
-                                      void* stream) {
+namespace {
+
+tvl_status decode_impl(float* out, const void* q, const void* k_new, const void* v_new,
+                       const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                       const int32_t* context_lens, int num_seqs, int num_q_heads,
+                       int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                       int max_blocks_per_seq, float scale, int partition_size, void* workspace,
+                       size_t workspace_bytes, void* stream) {
   long long records = 0;
   int pb = 0, ms = 0, ctas = 0;
   tvl_status st = decode_sizes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
@@ -304,6 +305,10 @@ tvl_status tvl_paged_attention_decode(float* out, const void* q, const void* k_c
     return fail(TVL_ERR_INVALID_ARG, "null pointer argument");
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return fail(TVL_ERR_INVALID_ARG, "out, q, k_cache and v_cache must be 16-byte aligned");
+  if ((k_new == nullptr) != (v_new == nullptr))
+    return fail(TVL_ERR_INVALID_ARG, "k_new and v_new must both be given");
+  if ((k_new && !aligned16(k_new)) || (v_new && !aligned16(v_new)))
+    return fail(TVL_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
   const size_t need = tvl::decode_workspace_bytes(records, num_q_heads, head_dim);
   if (need > 0) {
     if (!workspace || workspace_bytes < need)
@@ -318,6 +323,8 @@ tvl_status tvl_paged_attention_decode(float* out, const void* q, const void* k_c
   a.q = q;
   a.k_cache = k_cache;
   a.v_cache = v_cache;
+  a.k_new = k_new;
+  a.v_new = v_new;
   a.block_tables = block_tables;
   a.context_lens = context_lens;
   a.num_seqs = num_seqs;
@@ -336,6 +343,36 @@ tvl_status tvl_paged_attention_decode(float* out, const void* q, const void* k_c
   cudaError_t e = tvl::launch_decode(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return TVL_OK;
+}
+
+}  // namespace
+
+tvl_status tvl_paged_attention_decode(float* out, const void* q, const void* k_cache,
+                                      const void* v_cache, const int32_t* block_tables,
+                                      const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                      int num_kv_heads, int head_dim, int block_size,
+                                      int num_blocks, int max_blocks_per_seq, float scale,
+                                      int partition_size, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+  return decode_impl(out, q, nullptr, nullptr, k_cache, v_cache, block_tables, context_lens,
+                     num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                     max_blocks_per_seq, scale, partition_size, workspace, workspace_bytes,
+                     stream);
+}
+
+tvl_status tvl_paged_decode_step(float* out, const void* q, const void* k_new,
+                                 const void* v_new, void* k_cache, void* v_cache,
+                                 const int32_t* block_tables, const int32_t* context_lens,
+                                 int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int block_size, int num_blocks, int max_blocks_per_seq,
+                                 float scale, int partition_size, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  if (num_seqs > 0 && (!k_new || !v_new))
+    return fail(TVL_ERR_INVALID_ARG, "null k_new / v_new");
+  return decode_impl(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                     num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                     max_blocks_per_seq, scale, partition_size, workspace, workspace_bytes,
+                     stream);
 }
 
 tvl_status tvl_paged_attention_prefill(float* out, const void* q, const int32_t* query_start_loc,

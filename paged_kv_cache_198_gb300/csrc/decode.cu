@@ -81,6 +81,10 @@ struct Params {
   const __nv_bfloat16* q;
   const __nv_bfloat16* k_cache;
   const __nv_bfloat16* v_cache;
+  const __nv_bfloat16* k_new;     // fused write of each sequence's new token, or null
+  const __nv_bfloat16* v_new;
+  __nv_bfloat16* k_cache_w;       // k_cache / v_cache, writable (fused write only)
+  __nv_bfloat16* v_cache_w;
   const int32_t* block_tables;
   const int32_t* context_lens;
   int num_seqs, hq, hkv, num_blocks, max_blocks;
@@ -237,17 +241,37 @@ __device__ void producer(const Params& p, const Schedule& sc, uint8_t* smem, con
     }
     const int32_t* table = p.block_tables + static_cast<long long>(s) * p.max_blocks;
     int tbl = 0;
+    // Fused write: when this segment holds the sequence's last block, fetch
+    // the new token's K/V rows (this CTA's heads) now, so the loads have
+    // landed by the time the last block's stage is issued.
+    static_assert(kMaxHeadsPerCta * kRowBytes / 16 <= 64, "two 16-byte pieces a lane");
+    const int wchunks = hpc * kRowBytes / 16;          // 16-byte pieces per row, <= 64
+    uint4 wk[2], wv[2];
+    const bool fused_write = p.k_new != nullptr && e == nb;
+    if (fused_write) {
+      const size_t src = (static_cast<size_t>(s) * p.hkv + hg * hpc) * kD;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int c = lane + 32 * i;
+        if (c < wchunks) {
+          wk[i] = reinterpret_cast<const uint4*>(p.k_new + src)[c];
+          wv[i] = reinterpret_cast<const uint4*>(p.v_new + src)[c];
+        }
+      }
+    }
     for (long long blk = b; blk < e && ok; blk += BPS) {
       const int slot = static_cast<int>((blk - b) & 31);   // BPS divides 32
       if (slot == 0) tbl = (blk + lane < e) ? table[blk + lane] : 0;
       const int nstage = (e - blk < BPS) ? static_cast<int>(e - blk) : BPS;
       int phys[BPS];
+      bool last_ok = true;                               // stage's last block id valid
 #pragma unroll
       for (int i = 0; i < BPS; ++i) {
         phys[i] = __shfl_sync(kFull, tbl, slot + i);
         if (i < nstage && (phys[i] < 0 || phys[i] >= p.num_blocks)) {
           if (lane == 0) report(p.status, TVL_DEV_BAD_BLOCK_ID);
           phys[i] = 0;
+          if (i == nstage - 1) last_ok = false;
         }
       }
       int st;
@@ -270,6 +294,26 @@ __device__ void producer(const Params& p, const Schedule& sc, uint8_t* smem, con
         m.record = record;
         meta[st] = m;
         mbar_arrive_expect_tx(&full[st], 2 * nstage * blk_bytes + (first ? q_bytes : 0));
+      }
+      if (fused_write && blk + nstage == nb && last_ok) {
+        // The new token (position ctx - 1: the last block's row
+        // (ctx - 1) % BS) goes into the cache before the block is copied:
+        // generic stores, then a proxy fence so that the bulk copy (async
+        // proxy) reads them.
+        const int last = nstage == 1 ? phys[0] : phys[BPS - 1];
+        const size_t row =
+            ((static_cast<size_t>(last) * BS + (ctx - 1) % BS) * p.hkv + hg * hpc) * kD;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int c = lane + 32 * i;
+          if (c < wchunks) {
+            reinterpret_cast<uint4*>(p.k_cache_w + row)[c] = wk[i];
+            reinterpret_cast<uint4*>(p.v_cache_w + row)[c] = wv[i];
+          }
+        }
+        asm volatile("fence.proxy.async;" ::: "memory");
+        __syncwarp();
+        asm volatile("fence.proxy.async;" ::: "memory");
       }
       __syncwarp();
       if (whole_rows) {
@@ -924,6 +968,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   prm.q = static_cast<const __nv_bfloat16*>(a.q);
   prm.k_cache = static_cast<const __nv_bfloat16*>(a.k_cache);
   prm.v_cache = static_cast<const __nv_bfloat16*>(a.v_cache);
+  prm.k_new = static_cast<const __nv_bfloat16*>(a.k_new);
+  prm.v_new = static_cast<const __nv_bfloat16*>(a.v_new);
+  prm.k_cache_w = static_cast<__nv_bfloat16*>(const_cast<void*>(a.k_cache));
+  prm.v_cache_w = static_cast<__nv_bfloat16*>(const_cast<void*>(a.v_cache));
   prm.block_tables = a.block_tables;
   prm.context_lens = a.context_lens;
   prm.num_seqs = a.num_seqs;

@@ -62,6 +62,8 @@ struct DecodeArgs {
   const void* q;
   const void* k_cache;
   const void* v_cache;
+  const void* k_new;      // non-null: write each sequence's new token first (decode step)
+  const void* v_new;
   const int32_t* block_tables;
   const int32_t* context_lens;
   int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
