@@ -13,16 +13,16 @@
 // from the paged cache serves NH heads.  Warps:
 //   0..4NH-1  softmax, one warpgroup per head: thread r owns query row r
 //             (TMEM lane r).  Per 128-key tile it loads its 128 scores into
-//             registers, converting its share of the V tile bf16 -> fp16 in
-//             place while the loads fly (exact for |v| >= 2^-14; keys past
-//             the context become 0), and releases S at once so the next
-//             tile's Q K^T overlaps the rest.  It then computes
-//             P = 2^(S*scale*log2e - m) with packed fp32x2 arithmetic against
-//             a reference maximum m that moves only when a tile's maximum
-//             exceeds it by more than 2^8 (O in TMEM is then rescaled; exact,
-//             since one reference scales numerator and denominator), and
-//             stores P as fp16 into TMEM once the previous P.V has consumed
-//             the buffer.  At the end it normalises O and writes it out;
+//             registers and releases S at once, so the next tile's Q K^T
+//             overlaps the rest.  It computes P = 2^(S*scale*log2e - m) with
+//             packed fp32x2 arithmetic against a reference maximum m set by
+//             the first tile; only when a tile's row sum shows that some P
+//             nears the fp16 limit does it take the tile's maximum, move m
+//             and recompute P from the scores still in registers (O in TMEM
+//             is then rescaled; exact, since one reference scales numerator
+//             and denominator).  P is stored as fp16 into TMEM once the
+//             previous P.V has consumed the buffer.  At the end it
+//             normalises O and writes it out;
 //   4NH       producer: TMA loads of the Q tiles and, per 128-key tile, one
 //             box of bs tokens x 64 dims per physical block (K and V) found
 //             through the block table -- the paged gather; blocks past the
@@ -31,8 +31,10 @@
 //             shared memory) and O_h += P_h V (M 128, N 64, fp16, P read from
 //             TMEM, V an MN-major shared operand), fp32 accumulation.  The
 //             next tile's S is issued as soon as the softmax has released S,
-//             before this tile's P.V, so the tensor pipe works while P is
-//             computed.  Completion is signalled by tcgen05.commit.
+//             before this tile's P.V.  Completion is signalled by
+//             tcgen05.commit;
+//   4NH+2,+3  V conversion: each V tile bf16 -> fp16 in place (exact for
+//             |v| >= 2^-14; keys past the context become 0).
 // P and V go through fp16 rather than bf16 so that rounding P costs at most
 // 2^-11 relative (bf16 would cost 2^-8) -- the fp32-accumulated result stays
 // within 2e-3 of the exact attention even for rows with few keys.
@@ -55,7 +57,6 @@ constexpr int kD = 64;
 constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kStages = 3;
-constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr uint32_t kTileBytes = kBM * kD * 2;      // 16 KB: 128 rows x 128 B
@@ -68,7 +69,8 @@ struct Cfg {
   static constexpr int kSoftmaxWarps = 4 * NH;
   static constexpr int kProducerWarp = kSoftmaxWarps;
   static constexpr int kMmaWarp = kSoftmaxWarps + 1;
-  static constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+  static constexpr int kConvWarp = kSoftmaxWarps + 2;        // two V-conversion warps
+  static constexpr int kThreads = (kSoftmaxWarps + 4) * 32;
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKOff = NH * kTileBytes;
   static constexpr uint32_t kVOff = kKOff + kStages * kTileBytes;
@@ -79,6 +81,14 @@ struct Cfg {
   __device__ static uint32_t o_col(int h) { return NH * kBN + h * kD; }
   __device__ static uint32_t p_col(int h) { return NH * (kBN + kD) + h * (kBN / 2); }
 };
+
+// Register split of the two-head kernel: 12 warps launched with 168
+// registers each (64512); the producer / MMA / conversion warpgroup drops to
+// 64 and the two softmax warpgroups rise to 216, which holds a row's 128
+// scores and its 64 packed P together: 2 x 128 x 216 + 128 x 64 = 63488.
+// The host checks the launch allocation before the first launch.
+constexpr int kRegsSoftmax = 216;
+constexpr int kRegsAux = 64;
 
 struct Barriers {
   uint64_t q_full;
@@ -189,7 +199,7 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&B->kv_full[i], 1);
       mbar_init(&B->kv_empty[i], 1);
-      mbar_init(&B->v_ready[i], C::kSoftmaxWarps);
+      mbar_init(&B->v_ready[i], 2);
     }
     for (int i = 0; i < NH; ++i) {
       mbar_init(&B->s_full[i], 1);
@@ -210,6 +220,8 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = B->tmem_base;
 
+  if (warp >= C::kSoftmaxWarps) {
+  if constexpr (NH == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsAux));
   if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -306,7 +318,37 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
       if (!mbar_wait(&B->mma_done, 0)) report(p.status, kDevTimeout);
     }
   } else {
+    // ----------------------------------------------- V conversion (2 warps)
+    // V tile j bf16 -> fp16 in place, 16 bytes at a time (the swizzle only
+    // permutes 16-byte chunks within a 128-byte row, so a chunk's row is its
+    // offset / 128); keys past the context become 0.
+    const int t = (warp - C::kConvWarp) * 32 + lane;
+    for (int j = 0; j < n_kv; ++j) {
+      const int st = j % kStages;
+      const bool ok = wait_or_abort(&B->kv_full[st], (j / kStages) & 1, B, p);
+      if (__any_sync(kFull, !ok)) break;
+      uint8_t* vt = smem + C::kVOff + st * kTileBytes;
+#pragma unroll 4
+      for (int c = t; c < static_cast<int>(kTileBytes / 16); c += 64) {
+        uint4 w = *reinterpret_cast<const uint4*>(vt + c * 16);
+        if (j * kBN + (c >> 3) < ctx) {
+          w.x = bf16x2_to_half2(w.x);
+          w.y = bf16x2_to_half2(w.y);
+          w.z = bf16x2_to_half2(w.z);
+          w.w = bf16x2_to_half2(w.w);
+        } else {
+          w = make_uint4(0, 0, 0, 0);
+        }
+        *reinterpret_cast<uint4*>(vt + c * 16) = w;
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B->v_ready[st]);
+    }
+  }
+  } else {
     // ------------------------------------------------------------- softmax
+    if constexpr (NH == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     const int hh = warp >> 2;                           // head of this warpgroup
     const int wi = warp & 3;                            // TMEM lane quadrant
     const int r = wi * 32 + lane;                       // row == TMEM lane
@@ -315,50 +357,19 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
     const uint32_t o_addr = tmem + lane_off + C::o_col(hh);
     const uint32_t p_addr = tmem + lane_off + C::p_col(hh);
     const int qpos = pos_first + r;
-    // this thread's share of the V conversion: NH warpgroups split the rows
-    const int vrows = kBN / NH;
-    const int vrow = hh * vrows + (NH == 2 ? (r >> 1) : r);
-    const int vchunk0 = NH == 2 ? (r & 1) * 4 : 0;
-    const int vchunks = NH == 2 ? 4 : 8;
     const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
     float m_used = -INFINITY;                           // reference maximum (log2 units)
     float2 l2 = make_float2(0.f, 0.f);
     bool ok = true;
 
     for (int j = 0; j < n_kv && ok; ++j) {
-      const int st = j % kStages;
       const int key0 = j * kBN;
-      ok = wait_or_abort(&B->kv_full[st], (j / kStages) & 1, B, p) &&
-           wait_or_abort(&B->s_full[hh], j & 1, B, p);
+      ok = wait_or_abort(&B->s_full[hh], j & 1, B, p);
       if (__any_sync(kFull, !ok)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[4][32];                               // this row's 128 scores
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
-      // --- while those loads fly: V tile j bf16 -> fp16 in place (keys past
-      // the context -> 0), this warpgroup's share of the rows
-      {
-        uint8_t* vr = smem + C::kVOff + st * kTileBytes + vrow * 128;
-        const bool key_ok = key0 + vrow < ctx;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (i >= vchunks) break;
-          const int chunk = (vchunk0 + i) ^ (vrow & 7);
-          uint4 w = *reinterpret_cast<const uint4*>(vr + chunk * 16);
-          if (key_ok) {
-            w.x = bf16x2_to_half2(w.x);
-            w.y = bf16x2_to_half2(w.y);
-            w.z = bf16x2_to_half2(w.z);
-            w.w = bf16x2_to_half2(w.w);
-          } else {
-            w = make_uint4(0, 0, 0, 0);
-          }
-          *reinterpret_cast<uint4*>(vr + chunk * 16) = w;
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&B->v_ready[st]);
-      }
       tmem_ld_wait();
       // S_h is in registers: the next tile's Q K^T may overwrite it
       tc_fence_before();
@@ -369,72 +380,89 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
       const bool masked = (key0 + kBN - 1 > pos_first) || (key0 + kBN > ctx);
       const int limit = min(qpos, ctx - 1) - key0;     // last visible column
       // row maximum of the scaled scores of this tile
-      float mt;
-      if (masked) {
-        mt = -INFINITY;
+      auto tile_max = [&]() -> float {
+        float mt;
+        if (masked) {
+          mt = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float v = __uint_as_float(sr[c][e]) * p.scale_log2;
-            if (c * 32 + e > limit) v = -INFINITY;
-            mt = fmaxf(mt, v);
-          }
-      } else if (p.scale_log2 >= 0.f) {
-        float mx = -INFINITY;
+            for (int e = 0; e < 32; ++e) {
+              float v = __uint_as_float(sr[c][e]) * p.scale_log2;
+              if (c * 32 + e > limit) v = -INFINITY;
+              mt = fmaxf(mt, v);
+            }
+        } else if (p.scale_log2 >= 0.f) {
+          float mx = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            mx = max3(mx, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-        mt = mx * p.scale_log2;
-      } else {
-        float mn = INFINITY;
+            for (int e = 0; e < 32; e += 2)
+              mx = max3(mx, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+          mt = mx * p.scale_log2;
+        } else {
+          float mn = INFINITY;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            mn = min3(mn, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-        mt = mn * p.scale_log2;
-      }
-      // The reference maximum moves only when the tile's maximum exceeds it
-      // by more than 2^8, so every P <= 256 fits fp16; the result is exact
-      // either way because one reference scales numerator and denominator.
-      float f = 1.f;
-      const bool move = j == 0 ? true : mt > m_used + kRescaleLog2;
-      if (move) {
-        f = j == 0 ? 1.f : ex2(m_used - mt);
-        m_used = mt;
-      }
-      const float mref = m_used == -INFINITY ? 0.f : m_used;
-      const float2 nm2 = make_float2(-mref, -mref);
-      // P = 2^(s * scale * log2e - m) in registers, fp16 pairs
+            for (int e = 0; e < 32; e += 2)
+              mn = min3(mn, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+          mt = mn * p.scale_log2;
+        }
+        return mt;
+      };
       uint32_t pk[2][32];
-      float2 tsum = make_float2(0.f, 0.f);
-      if (masked) {
+      // P = 2^(s * scale * log2e - m) as fp16 pairs; returns the fp32 row sum
+      auto make_p = [&](float mref) -> float2 {
+        const float2 nm2 = make_float2(-mref, -mref);
+        float2 tsum = make_float2(0.f, 0.f);
+        if (masked) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float2 x = make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-            x = __ffma2_rn(x, sl2, nm2);
-            if (c * 32 + e > limit) x.x = -INFINITY;
-            if (c * 32 + e + 1 > limit) x.y = -INFINITY;
-            const float2 pv = make_float2(ex2(x.x), ex2(x.y));
-            tsum = __fadd2_rn(tsum, pv);
-            pk[c >> 1][(c & 1) * 16 + e / 2] = pack_half2(pv.x, pv.y);
-          }
+            for (int e = 0; e < 32; e += 2) {
+              float2 x = make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+              x = __ffma2_rn(x, sl2, nm2);
+              if (c * 32 + e > limit) x.x = -INFINITY;
+              if (c * 32 + e + 1 > limit) x.y = -INFINITY;
+              const float2 pv = make_float2(ex2(x.x), ex2(x.y));
+              tsum = __fadd2_rn(tsum, pv);
+              pk[c >> 1][(c & 1) * 16 + e / 2] = pack_half2(pv.x, pv.y);
+            }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float2 x = make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+              x = __ffma2_rn(x, sl2, nm2);
+              const float2 pv = make_float2(ex2(x.x), ex2(x.y));
+              tsum = __fadd2_rn(tsum, pv);
+              pk[c >> 1][(c & 1) * 16 + e / 2] = pack_half2(pv.x, pv.y);
+            }
+        }
+        return tsum;
+      };
+      float f = 1.f;
+      bool move = false;
+      float2 tsum;
+      if (j == 0) {
+        m_used = tile_max();
+        tsum = make_p(m_used == -INFINITY ? 0.f : m_used);
       } else {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float2 x = make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-            x = __ffma2_rn(x, sl2, nm2);
-            const float2 pv = make_float2(ex2(x.x), ex2(x.y));
-            tsum = __fadd2_rn(tsum, pv);
-            pk[c >> 1][(c & 1) * 16 + e / 2] = pack_half2(pv.x, pv.y);
+        // P straight from the reference maximum; only a row sum that shows
+        // some P near the fp16 limit (65504) calls for the tile's maximum
+        tsum = make_p(m_used == -INFINITY ? 0.f : m_used);
+        const float ts = tsum.x + tsum.y;
+        move = !(ts <= 60000.f);
+        if (__any_sync(kFull, move)) {
+          if (move) {
+            const float m_new = fmaxf(m_used, tile_max());
+            f = ex2(m_used - m_new);
+            m_used = m_new;
           }
+          tsum = make_p(m_used == -INFINITY ? 0.f : m_used);
+        }
       }
       // P_h(j-1) must have been consumed (and O_h(j-1) complete) before P_h
       // is overwritten and O_h rescaled
@@ -530,6 +558,15 @@ cudaError_t launch_nh(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<NH>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
+  if (NH == 2) {
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, prefill_kernel<NH>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * C::kThreads < 2 * 128 * kRegsSoftmax + 128 * kRegsAux) {
+      set_last_error("prefill kernel register allocation smaller than its register split");
+      return cudaErrorInvalidConfiguration;
+    }
+  }
   dim3 grid(p.n_qtiles, p.hq / NH, num_seqs);
   return launch_pdl(prefill_kernel<NH>, grid, dim3(C::kThreads), C::kSmemBytes, stream, tq, tk,
                     tv, p);
