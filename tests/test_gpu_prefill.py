@@ -88,6 +88,37 @@ def test_prefill_short_rows_unit_variance():
     assert_close(got, oracle_prefill(wl), "short rows N(0,1)")
 
 
+@pytest.mark.parametrize("rise", [20.0, -20.0])
+def test_prefill_scores_rising_along_the_context(rise):
+    """Scores that grow (or fall) by ~20 along each row: later key tiles beat
+    the first tile's maximum by far more than fp16 P can absorb, so the kernel
+    must move its reference maximum (and rescale O) on later tiles; falling
+    scores drive P of later tiles toward 0 instead."""
+    wl = W.make_prefill(726, [1000, 37], [130, 300], num_q_heads=8, num_kv_heads=2,
+                        block_size=16)
+    bs = wl.block_size
+    q = wl.q.float()
+    q[:, :, 0] = 8.0
+    wl.q = q.to(torch.bfloat16)
+    kc = wl.k_cache.float().view(-1, wl.num_kv_heads, wl.head_dim)
+    kn = wl.k_new.float()
+    for s in range(wl.num_seqs):
+        ctx = int(wl.context_lens[s])
+        pre = int(wl.prefix_lens[s])
+        q0 = int(wl.query_start_loc[s])
+        for j in range(ctx):
+            val = rise * j / ctx / (8.0 * wl.scale)     # score component = rise * j / ctx
+            if j < pre:
+                kc[W.slot_of(wl.block_tables, s, j, bs), :, 0] = val
+            else:
+                kn[q0 + j - pre, :, 0] = val
+    wl.k_cache = kc.view(wl.k_cache.shape).to(torch.bfloat16)
+    wl.k_new = kn.to(torch.bfloat16)
+    got, _ = gpu_prefill(wl)
+    assert_close(got, oracle_prefill(wl), f"rising {rise}")
+    assert_clean_status()
+
+
 def test_prefill_poisoned_unused_slots():
     wl = W.make_prefill(721, [3, 40, 200], [10, 100, 60], num_q_heads=8, num_kv_heads=2,
                         block_size=32)
