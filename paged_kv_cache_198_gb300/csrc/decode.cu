@@ -804,6 +804,7 @@ struct MergeParams {
 
 constexpr int kMergeWarps = 4;       // one warp per query head
 constexpr int kMergeMaxRecords = 512; // record indices staged per pass
+constexpr int kMergeBatch = 16;       // records whose loads are in flight together
 
 __device__ __forceinline__ int merge_ctx(const MergeParams& p, int s) {
   int c = p.context_lens[s];
@@ -896,15 +897,31 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
     o0 *= f;
     o1 *= f;
     mx = m_new;
-#pragma unroll 4
-    for (int k = 0; k < n; ++k) {
-      const int r = recs[k];
-      if (r < 0) continue;
-      const long long row = static_cast<long long>(r) * p.hq + h;
-      const float wgt = ex2(p.ws.m[row] - mx);
-      den += wgt * p.ws.l[row];
-      o0 += wgt * p.ws.acc[row * kD + lane];
-      o1 += wgt * p.ws.acc[row * kD + lane + 32];
+    // 16 records at a time, every load of a batch issued before any is used
+    // (a sequence split into 512-token windows has hundreds of records)
+    for (int k0 = 0; k0 < n; k0 += kMergeBatch) {
+      float mv[kMergeBatch], lv[kMergeBatch], a0[kMergeBatch], a1[kMergeBatch];
+      bool have[kMergeBatch];
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) {
+        const int r = k0 + u < n ? recs[k0 + u] : -1;
+        have[u] = r >= 0;
+        mv[u] = lv[u] = a0[u] = a1[u] = 0.f;
+        if (have[u]) {
+          const long long row = static_cast<long long>(r) * p.hq + h;
+          mv[u] = p.ws.m[row];
+          lv[u] = p.ws.l[row];
+          a0[u] = p.ws.acc[row * kD + lane];
+          a1[u] = p.ws.acc[row * kD + lane + 32];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) {
+        const float wgt = have[u] ? ex2(mv[u] - mx) : 0.f;
+        den = fmaf(wgt, lv[u], den);
+        o0 = fmaf(wgt, a0[u], o0);
+        o1 = fmaf(wgt, a1[u], o1);
+      }
     }
   }
   if (h >= p.hq) return;
