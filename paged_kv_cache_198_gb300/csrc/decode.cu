@@ -802,7 +802,8 @@ struct MergeParams {
   uint32_t* status;
 };
 
-constexpr int kMergeWarps = 4;       // one warp per query head
+constexpr int kMergeHeads = 4;       // query heads per CTA
+constexpr int kMergeMaxParts = 4;    // warps per head when sequences have many records
 constexpr int kMergeMaxRecords = 512; // record indices staged per pass
 constexpr int kMergeBatch = 16;       // records whose loads are in flight together
 
@@ -817,12 +818,17 @@ __device__ __forceinline__ int merge_ctx(const MergeParams& p, int s) {
 // Small (128 threads, few registers) so that its CTAs fit beside the decode
 // CTAs and run their prologue -- the record list, which depends only on the
 // context lengths -- while the decode finishes.
-__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeParams p) {
+__global__ void __launch_bounds__(kMergeHeads * kMergeMaxParts * 32)
+    merge_kernel(const MergeParams p) {
   __shared__ long long tmp[32];
   __shared__ int recs[kMergeMaxRecords];
+  __shared__ float part_m[kMergeMaxParts][kMergeHeads], part_l[kMergeMaxParts][kMergeHeads];
+  __shared__ float part_o[kMergeMaxParts][kMergeHeads][kD];
   const int s = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int h = blockIdx.y * kMergeWarps + warp;
+  const int parts = static_cast<int>(blockDim.x) / (32 * kMergeHeads);
+  const int hw = warp % kMergeHeads, part = warp / kMergeHeads;
+  const int h = blockIdx.y * kMergeHeads + hw;
   const long long nb = (merge_ctx(p, s) + p.bs - 1) / p.bs;
   const bool fixed = p.partition_blocks > 0;
 
@@ -833,7 +839,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
   } else {
     if (nb == 0) {
       grid_dependency_wait();
-      if (h < p.hq) {
+      if (h < p.hq && part == 0) {
         float* dst = p.out + (static_cast<long long>(s) * p.hq + h) * kD;
         dst[lane] = 0.f;
         dst[lane + 32] = 0.f;
@@ -883,28 +889,30 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
       waited = true;
     }
     if (h >= p.hq) continue;
-    // running maximum over this pass's records (lanes split the records)
+    // this warp's slice of the pass's records
+    const int k_lo = n * part / parts, k_hi = n * (part + 1) / parts;
+    // running maximum over the slice (lanes split the records)
     float pm = -INFINITY;
-    for (int k = lane; k < n; k += 32) {
+    for (int k = k_lo + lane; k < k_hi; k += 32) {
       const int r = recs[k];
       if (r >= 0) pm = fmaxf(pm, p.ws.m[static_cast<long long>(r) * p.hq + h]);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, o));
     const float m_new = fmaxf(mx, pm);
-    const float f = ex2(mx - m_new);     // 0 on the first pass
+    const float f = m_new == -INFINITY ? 1.f : ex2(mx - m_new);   // 0 on the first pass
     den *= f;
     o0 *= f;
     o1 *= f;
     mx = m_new;
     // 16 records at a time, every load of a batch issued before any is used
     // (a sequence split into 512-token windows has hundreds of records)
-    for (int k0 = 0; k0 < n; k0 += kMergeBatch) {
+    for (int k0 = k_lo; k0 < k_hi; k0 += kMergeBatch) {
       float mv[kMergeBatch], lv[kMergeBatch], a0[kMergeBatch], a1[kMergeBatch];
       bool have[kMergeBatch];
 #pragma unroll
       for (int u = 0; u < kMergeBatch; ++u) {
-        const int r = k0 + u < n ? recs[k0 + u] : -1;
+        const int r = k0 + u < k_hi ? recs[k0 + u] : -1;
         have[u] = r >= 0;
         mv[u] = lv[u] = a0[u] = a1[u] = 0.f;
         if (have[u]) {
@@ -922,6 +930,27 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
         o0 = fmaf(wgt, a0[u], o0);
         o1 = fmaf(wgt, a1[u], o1);
       }
+    }
+  }
+  if (parts > 1) {
+    // combine the slices of each head:  M = max m_i, sum 2^(m_i - M) (.)_i
+    if (lane == 0) {
+      part_m[part][hw] = mx;
+      part_l[part][hw] = den;
+    }
+    part_o[part][hw][lane] = o0;
+    part_o[part][hw][lane + 32] = o1;
+    __syncthreads();
+    if (part != 0) return;
+    float mm = -INFINITY;
+    for (int i = 0; i < parts; ++i) mm = fmaxf(mm, part_m[i][hw]);
+    den = o0 = o1 = 0.f;
+    for (int i = 0; i < parts; ++i) {
+      const float mi = part_m[i][hw];
+      const float w = mi == -INFINITY ? 0.f : ex2(mi - mm);
+      den = fmaf(w, part_l[i][hw], den);
+      o0 = fmaf(w, part_o[i][hw][lane], o0);
+      o1 = fmaf(w, part_o[i][hw][lane + 32], o1);
     }
   }
   if (h >= p.hq) return;
@@ -1046,8 +1075,11 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   mp.balanced_ctas = a.balanced_ctas;
   mp.ws = a.ws;
   mp.status = a.status;
-  dim3 mgrid(a.num_seqs, (a.num_q_heads + kMergeWarps - 1) / kMergeWarps);
-  return launch_pdl(merge_kernel, mgrid, dim3(kMergeWarps * 32), 0, stream, mp);
+  dim3 mgrid(a.num_seqs, (a.num_q_heads + kMergeHeads - 1) / kMergeHeads);
+  // many records per sequence (fixed windows over long contexts): four warps
+  // per head, each merging a quarter of the records
+  const int parts = a.partition_blocks > 0 && a.max_splits > 64 ? kMergeMaxParts : 1;
+  return launch_pdl(merge_kernel, mgrid, dim3(kMergeHeads * parts * 32), 0, stream, mp);
 }
 
 }  // namespace tvl
