@@ -275,6 +275,21 @@ def bench_decode(wl, args, rank, world, device):
         torch.distributed.barrier()
     elapsed_ms = start.elapsed_time(stop)
 
+    # the decode alone (tvl_paged_attention_decode over the written caches),
+    # back to back, for the decode-only figure
+    d0 = torch.cuda.Event(enable_timing=True)
+    d1 = torch.cuda.Event(enable_timing=True)
+    n_dec = max(1, min(args.steps, 2000))
+    d0.record(stream)
+    for i in range(n_dec):
+        t = sets[i % copies]
+        tvl.paged_attention_decode(out, t["q"], t["k_cache"], t["v_cache"], t["block_tables"],
+                                   t["context_lens"], wl.scale, partition_size=part,
+                                   workspace=ws)
+    d1.record(stream)
+    torch.cuda.synchronize(device)
+    decode_only_ms = d0.elapsed_time(d1) / n_dec
+
     # End to end through the public API: every step copies its inputs from
     # pinned host memory, makes the call and reads its output back.  Copies
     # run on a second stream with two buffer sets, so the H2D of step i+1 and
@@ -330,6 +345,7 @@ def bench_decode(wl, args, rank, world, device):
         raise RuntimeError("device status word set during timing")
     return {
         "elapsed_ms": elapsed_ms, "decode_ms": elapsed_ms / args.steps, "e2e_ms": e2e_ms,
+        "decode_only_ms": decode_only_ms,
         "h2d": h2d, "d2h": d2h, "copies": copies, "clocks": clocks.summary(host_t0, host_t1),
         "launches_per_step": 2 if (part == 0 or wl.max_blocks_per_seq * wl.block_size > part)
         else 1,
@@ -617,6 +633,13 @@ def main():
                           "the H2D of step i+1 and the D2H of step i-1 overlap step i"},
         "gpu_launches": r["launches_per_step"] * args.steps,
         "clocks": r["clocks"],
+        "decode_only": {
+            "call": "tvl_paged_attention_decode (decode + merge, the write not included)",
+            "ms_per_call": round(r["decode_only_ms"], 5),
+            "achieved_gbs": round(decode_algorithmic_bytes(wl) / (r["decode_only_ms"] / 1e3)
+                                  / 1e9, 1),
+            "frac": round(decode_algorithmic_bytes(wl) / (r["decode_only_ms"] / 1e3) / 1e9
+                          / hbm_peak, 4)},
     }
     if not args.no_cpu_baseline and world == 1:
         per, cores, reps = cpu_baseline_decode(wl)
