@@ -464,7 +464,7 @@ def prefill_line(wl, args, r, bf16_sus, peak_src):
         "e2e": {"value": round(flops / (r["e2e_ms_per_step"] / 1e3) / 1e12, 2),
                 "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"]},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,     # the step's region; the kernel-only one adds K more
         "clocks": r["clocks"],
     }
 
