@@ -291,9 +291,10 @@ def bench_decode(wl, args, rank, world, device):
     decode_only_ms = d0.elapsed_time(d1) / n_dec
 
     # End to end through the public API: every step copies its inputs from
-    # pinned host memory, makes the call and reads its output back.  Copies
-    # run on a second stream with two buffer sets, so the H2D of step i+1 and
-    # the D2H of step i-1 overlap step i (double buffering).
+    # pinned host memory (one packed H2D), makes the call and reads its output
+    # back.  H2D and D2H run on two copy streams (separate copy engines) with
+    # two buffer sets, so the H2D of step i+1 and the D2H of step i-1 overlap
+    # step i (double buffering).
     host = pack_pinned({k: v for k, v in W.to_device(wl, "cpu").items()
                         if k in ("q", "k_new", "v_new", "block_tables", "context_lens")})
     out_host = [torch.empty(s, hq, d, dtype=torch.float32).pin_memory() for _ in range(2)]
@@ -302,6 +303,7 @@ def bench_decode(wl, args, rank, world, device):
     dev_in = [unpack_views(host, torch.empty_like(host["buf"], device=device)) for _ in range(2)]
     outs = [torch.empty(s, hq, d, dtype=torch.float32, device=device) for _ in range(2)]
     copy_stream = torch.cuda.Stream(device)
+    d2h_stream = torch.cuda.Stream(device)
     ev = lambda: torch.cuda.Event()                      # noqa: E731
     in_ready, done, out_read = [ev(), ev()], [ev(), ev()], [ev(), ev()]
     used = [False, False]
@@ -322,10 +324,10 @@ def bench_decode(wl, args, rank, world, device):
                               dev_in[b]["context_lens"], wl.scale, partition_size=part,
                               workspace=ws)
         done[b].record(stream)
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(done[b])
+        with torch.cuda.stream(d2h_stream):
+            d2h_stream.wait_event(done[b])
             out_host[b].copy_(outs[b], non_blocking=True)
-            out_read[b].record(copy_stream)
+            out_read[b].record(d2h_stream)
         used[b] = True
 
     for i in range(args.warmup):
@@ -398,39 +400,65 @@ def bench_prefill(wl, args, device):
         time.sleep(0.1)
     if tvl.get_device_status() != 0:
         raise RuntimeError("device status word set during timing")
-    host = {k: base[k].cpu().pin_memory() for k in ("q", "k_new", "v_new", "slot_mapping",
-                                                    "query_start_loc", "block_tables",
-                                                    "context_lens")}
-    out_host = torch.empty(tuple(wl.q.shape), dtype=torch.float32).pin_memory()
-    dev_in = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    # End to end: each step copies its inputs from pinned host memory (one
+    # packed H2D), writes the chunk, runs the prefill and reads the output
+    # back.  H2D and D2H run on two copy streams (the two directions use
+    # separate copy engines) with two buffer sets, so step i's compute
+    # overlaps the H2D of step i+1 and the D2H of step i-1.
+    host = pack_pinned({k: base[k].cpu() for k in ("q", "k_new", "v_new", "slot_mapping",
+                                                   "query_start_loc", "block_tables",
+                                                   "context_lens")})
+    out_host = [torch.empty(tuple(wl.q.shape), dtype=torch.float32).pin_memory()
+                for _ in range(2)]
+    dev_in = [unpack_views(host, torch.empty_like(host["buf"], device=device)) for _ in range(2)]
+    outs = [torch.empty(tuple(wl.q.shape), dtype=torch.float32, device=device) for _ in range(2)]
+    h2d_stream = torch.cuda.Stream(device)
+    d2h_stream = torch.cuda.Stream(device)
+    ev = lambda: torch.cuda.Event()                      # noqa: E731
+    in_ready, done, out_read = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    used = [False, False]
 
-    def e2e_step(t):
-        for k, v in host.items():
-            dev_in[k].copy_(v, non_blocking=True)
-        tvl.paged_kv_write(dev_in["k_new"], dev_in["v_new"], t["k_cache"], t["v_cache"],
-                           dev_in["slot_mapping"])
-        tvl.paged_attention_prefill(out, dev_in["q"], dev_in["query_start_loc"], t["k_cache"],
-                                    t["v_cache"], dev_in["block_tables"],
-                                    dev_in["context_lens"], wl.scale, wl.max_q_len)
-        out_host.copy_(out, non_blocking=True)
+    def e2e_step(i):
+        b = i % 2
+        with torch.cuda.stream(h2d_stream):
+            if used[b]:
+                h2d_stream.wait_event(done[b])           # step i-2 has read these inputs
+            dev_in[b]["buf"].copy_(host["buf"], non_blocking=True)
+            in_ready[b].record(h2d_stream)
+        stream.wait_event(in_ready[b])
+        if used[b]:
+            stream.wait_event(out_read[b])               # step i-2's output was read back
+        t, d = sets[i % copies], dev_in[b]
+        tvl.paged_kv_write(d["k_new"], d["v_new"], t["k_cache"], t["v_cache"], d["slot_mapping"])
+        tvl.paged_attention_prefill(outs[b], d["q"], d["query_start_loc"], t["k_cache"],
+                                    t["v_cache"], d["block_tables"], d["context_lens"],
+                                    wl.scale, wl.max_q_len)
+        done[b].record(stream)
+        with torch.cuda.stream(d2h_stream):
+            d2h_stream.wait_event(done[b])
+            out_host[b].copy_(outs[b], non_blocking=True)
+            out_read[b].record(d2h_stream)
+        used[b] = True
 
     for i in range(args.warmup):
-        e2e_step(sets[i % copies])
+        e2e_step(i)
     torch.cuda.synchronize(device)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    e2e_steps = max(1, min(args.steps, 200))
+    h2d_stream.wait_event(e0)
+    e2e_steps = max(2, min(args.steps, 200))
     for i in range(e2e_steps):
-        e2e_step(sets[i % copies])
+        e2e_step(args.warmup + i)
+    stream.wait_event(out_read[(args.warmup + e2e_steps - 1) % 2])
     e1.record(stream)
     torch.cuda.synchronize(device)
     return {
         "elapsed_ms": start.elapsed_time(stop),
         "kernel_ms": k0.elapsed_time(k1) / args.steps,
         "e2e_ms_per_step": e0.elapsed_time(e1) / e2e_steps,
-        "h2d": sum(v.numel() * v.element_size() for v in host.values()),
-        "d2h": out_host.numel() * out_host.element_size(), "copies": copies,
+        "h2d": host["nbytes"],
+        "d2h": out_host[0].numel() * out_host[0].element_size(), "copies": copies,
         "clocks": clocks.summary(host_t0, host_t1),
     }
 
@@ -629,8 +657,8 @@ def main():
         },
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"], "ms_per_step": round(e2e_ms / args.steps, 4),
-                "copies": "pinned host buffers, a copy stream and two device buffer sets: "
-                          "the H2D of step i+1 and the D2H of step i-1 overlap step i"},
+                "copies": "pinned host buffers, H2D and D2H streams and two device buffer "
+                          "sets: the H2D of step i+1 and the D2H of step i-1 overlap step i"},
         "gpu_launches": r["launches_per_step"] * args.steps,
         "clocks": r["clocks"],
         "decode_only": {

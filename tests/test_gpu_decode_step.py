@@ -88,3 +88,24 @@ def test_decode_step_bad_last_block_is_reported_and_not_written():
     kw, _ = oracle.kv_write(wl.k_cache, wl.v_cache, wl.k_new[:1], wl.v_new[:1],
                             wl.slot_mapping[:1])
     assert np.array_equal(bits_of(k1), kw)
+
+
+@pytest.mark.parametrize("name", ["llama1b_decode", "continuous_batch"])
+def test_decode_step_full_size_as_benchmarked(name):
+    """The benchmarked call at full size: the Llama-1B-shaped batch and the
+    continuous batch, balanced split, one new token per sequence."""
+    wl = W.named(name, 0)
+    assert wl.k_new.shape[0] == wl.q.shape[0]
+    t = W.to_device(wl, DEV)
+    s, hq, d = wl.q.shape
+    out = torch.empty(s, hq, d, dtype=torch.float32, device=DEV)
+    tvl.paged_decode_step(out, t["q"], t["k_new"], t["v_new"], t["k_cache"], t["v_cache"],
+                          t["block_tables"], t["context_lens"], wl.scale)
+    torch.cuda.synchronize()
+    kw, vw = oracle.kv_write(wl.k_cache, wl.v_cache, wl.k_new, wl.v_new, wl.slot_mapping)
+    assert np.array_equal(bits_of(t["k_cache"]), kw)
+    assert np.array_equal(bits_of(t["v_cache"]), vw)
+    ref = oracle.decode(wl.q, kw.reshape(wl.k_cache.shape), vw.reshape(wl.v_cache.shape),
+                        wl.block_tables, wl.context_lens, wl.scale)
+    assert_close(out.double().cpu().numpy(), ref, name)
+    assert_clean_status()
