@@ -82,3 +82,25 @@ def test_validation_rejects_before_any_cuda_call(lib):
     rc = lib.tvl_paged_attention_decode_workspace_size(4, 24, 8, 64, 16, 16, 512,
                                                        ctypes.byref(size))
     assert rc == tvl.ERR_UNSUPPORTED
+
+
+def test_decode_step_validation_before_any_cuda_call(lib):
+    import paged_kv_cache_198_gb300 as tvl
+
+    P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.tvl_paged_decode_step.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P,
+                                          SZ, P]
+    lib.tvl_paged_decode_step.restype = I
+    d = P(256)
+    # no new K / V for a step with sequences
+    rc = lib.tvl_paged_decode_step(d, d, None, None, d, d, d, d, 4, 32, 8, 64, 16, 64, 16,
+                                   0.125, 256, None, 0, None)
+    assert rc == tvl.ERR_INVALID_ARG
+    # misaligned new K
+    rc = lib.tvl_paged_decode_step(d, d, P(258), d, d, d, d, d, 4, 32, 8, 64, 16, 64, 16,
+                                   0.125, 256, None, 0, None)
+    assert rc == tvl.ERR_INVALID_ARG
+    # unsupported block size is reported as such
+    rc = lib.tvl_paged_decode_step(d, d, d, d, d, d, d, d, 4, 32, 8, 64, 24, 64, 16,
+                                   0.125, 240, None, 0, None)
+    assert rc == tvl.ERR_UNSUPPORTED
