@@ -891,22 +891,10 @@ __global__ void __launch_bounds__(kMergeHeads * kMergeMaxParts * 32)
     if (h >= p.hq) continue;
     // this warp's slice of the pass's records
     const int k_lo = n * part / parts, k_hi = n * (part + 1) / parts;
-    // running maximum over the slice (lanes split the records)
-    float pm = -INFINITY;
-    for (int k = k_lo + lane; k < k_hi; k += 32) {
-      const int r = recs[k];
-      if (r >= 0) pm = fmaxf(pm, p.ws.m[static_cast<long long>(r) * p.hq + h]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, o));
-    const float m_new = fmaxf(mx, pm);
-    const float f = m_new == -INFINITY ? 1.f : ex2(mx - m_new);   // 0 on the first pass
-    den *= f;
-    o0 *= f;
-    o1 *= f;
-    mx = m_new;
     // 16 records at a time, every load of a batch issued before any is used
-    // (a sequence split into 512-token windows has hundreds of records)
+    // (a sequence split into 512-token windows has hundreds of records); the
+    // batch's maximum moves the running one, as in the online softmax, so
+    // one memory round trip serves a batch
     for (int k0 = k_lo; k0 < k_hi; k0 += kMergeBatch) {
       float mv[kMergeBatch], lv[kMergeBatch], a0[kMergeBatch], a1[kMergeBatch];
       bool have[kMergeBatch];
@@ -914,7 +902,8 @@ __global__ void __launch_bounds__(kMergeHeads * kMergeMaxParts * 32)
       for (int u = 0; u < kMergeBatch; ++u) {
         const int r = k0 + u < k_hi ? recs[k0 + u] : -1;
         have[u] = r >= 0;
-        mv[u] = lv[u] = a0[u] = a1[u] = 0.f;
+        mv[u] = -INFINITY;
+        lv[u] = a0[u] = a1[u] = 0.f;
         if (have[u]) {
           const long long row = static_cast<long long>(r) * p.hq + h;
           mv[u] = p.ws.m[row];
@@ -923,6 +912,15 @@ __global__ void __launch_bounds__(kMergeHeads * kMergeMaxParts * 32)
           a1[u] = p.ws.acc[row * kD + lane + 32];
         }
       }
+      float mb = mx;
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) mb = fmaxf(mb, mv[u]);
+      if (mb == -INFINITY) continue;                  // no record in this batch
+      const float f = ex2(mx - mb);                   // 0 while mx is -inf
+      den *= f;
+      o0 *= f;
+      o1 *= f;
+      mx = mb;
 #pragma unroll
       for (int u = 0; u < kMergeBatch; ++u) {
         const float wgt = have[u] ? ex2(mv[u] - mx) : 0.f;
