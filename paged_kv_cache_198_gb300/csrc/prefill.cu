@@ -56,7 +56,7 @@ namespace {
 constexpr int kD = 64;
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-constexpr int kStages = 3;
+constexpr int kStages = 5;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr uint32_t kTileBytes = kBM * kD * 2;      // 16 KB: 128 rows x 128 B
