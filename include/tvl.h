@@ -1,8 +1,10 @@
 /*
  * tvl.h -- C ABI of libtvl.so, a GB300 (sm_103a) implementation of the paged
  * attention hot path: the slot-mapped paged KV-cache write, PagedAttention
- * decode (single pass or split-K with a log-sum-exp merge) and chunked causal
- * prefill over a cached prefix.
+ * decode (single pass or split-K with a log-sum-exp merge), the two fused
+ * into one decode-step call, and chunked causal prefill over a cached
+ * prefix; around them the rotary embedding fused into the write, block
+ * copies for copy-on-write, and a host block allocator.
  *
  * Sources of the method (web pages on tiny-vLLM and nano-vLLM):
  *   [tiny-vllm README]  "tiny-vllm" README, Korean translation: feature list
