@@ -78,6 +78,8 @@ typedef enum {
 #define TVL_DEV_BAD_BLOCK_ID    0x2  /* block table entry outside [0, NB)        */
 #define TVL_DEV_BAD_CONTEXT_LEN 0x4  /* context length < 0 or > MB * bs          */
 #define TVL_DEV_BAD_QUERY_LEN   0x8  /* prefill: query length > context length   */
+#define TVL_DEV_TIMEOUT         0x10 /* a kernel's bounded wait gave up (~1 s);
+                                        its CTA left after its copies landed    */
 
 /*
  * Paged KV write [tiny-vllm README, curriculum "Paged KV cache" and "Why KV
@@ -333,6 +335,16 @@ const char* tvl_last_error(void);
  * set (the bits go to *bits if bits != NULL), TVL_ERR_CUDA on a CUDA error.
  */
 tvl_status tvl_get_device_status(void* stream, uint32_t* bits);
+
+/*
+ * Self-test of the kernels' bounded waits (no counterpart on the pages).  It
+ * launches one CTA that waits, with the same bounded mbarrier wait the
+ * kernels use, on a barrier nothing arrives at: after the wait's limit (about
+ * one second) it gives up and sets TVL_DEV_TIMEOUT in the status word, and
+ * the context stays usable.  Asynchronous on `stream`; tests use it to check
+ * that a wait that is never satisfied cannot hang the GPU.
+ */
+tvl_status tvl_selftest_bounded_wait(void* stream);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int tvl_version(void);

@@ -23,7 +23,7 @@ __all__ = [
     "rope_paged_kv_write",
     "paged_attention_decode_workspace_size", "paged_attention_prefill", "get_device_status",
     "version", "library_path", "DEV_BAD_SLOT", "DEV_BAD_BLOCK_ID", "DEV_BAD_CONTEXT_LEN",
-    "DEV_BAD_QUERY_LEN", "DEV_TIMEOUT",
+    "DEV_BAD_QUERY_LEN", "DEV_TIMEOUT", "selftest_bounded_wait", "paged_decode_step",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -70,6 +70,8 @@ def _load():
             lib.tvl_paged_decode_step.argtypes = [
                 P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, SZ, P]
             lib.tvl_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+            lib.tvl_selftest_bounded_wait.argtypes = [P]
+            lib.tvl_selftest_bounded_wait.restype = I
             for name in ("tvl_paged_kv_write", "tvl_paged_attention_decode_workspace_size",
                          "tvl_paged_attention_decode", "tvl_paged_attention_prefill",
                          "tvl_paged_decode_step", "tvl_get_device_status"):
@@ -297,6 +299,12 @@ def paged_attention_prefill(out, q, query_start_loc, k_cache, v_cache, block_tab
             _ptr(block_tables), _ptr(context_lens), s, tq, int(max_q_len), hq, hkv, d, bs, nb,
             mb, float(scale), _stream(stream)))
     return out
+
+
+def selftest_bounded_wait(stream=None) -> None:
+    """Launches one CTA whose bounded wait is never satisfied: it gives up
+    after about a second and sets DEV_TIMEOUT (tvl_selftest_bounded_wait)."""
+    _check(_load().tvl_selftest_bounded_wait(_stream(stream)))
 
 
 def get_device_status(stream=None) -> int:

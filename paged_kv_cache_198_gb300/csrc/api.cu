@@ -148,6 +148,15 @@ const char* tvl_last_error(void) { return g_last_error.c_str(); }
 
 int tvl_version(void) { return 100; }
 
+tvl_status tvl_selftest_bounded_wait(void* stream) {
+  uint32_t* word = nullptr;
+  tvl_status st = status_word(&word);
+  if (st != TVL_OK) return st;
+  cudaError_t e = tvl::launch_selftest_wait(word, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return TVL_OK;
+}
+
 tvl_status tvl_get_device_status(void* stream, uint32_t* bits) {
   uint32_t* word = nullptr;
   tvl_status st = status_word(&word);

@@ -86,6 +86,9 @@ DecodeWorkspace decode_workspace_carve(void* base, long long records, int num_q_
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
+// One CTA waiting on an mbarrier nothing arrives at (tvl_selftest_bounded_wait).
+cudaError_t launch_selftest_wait(uint32_t* status, cudaStream_t stream);
+
 struct PrefillArgs {
   float* out;
   const void* q;
