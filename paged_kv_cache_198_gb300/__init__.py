@@ -126,18 +126,44 @@ def _ptr(t) -> ctypes.c_void_p:
 
 
 def _need(t: torch.Tensor, name: str, dtype, ndim=None, device=None):
+    """Checks one argument; `device` is a torch.device or a CUDA device index.
+    Cheap on the common path (it runs for every tensor of every call)."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if not t.is_cuda:
+    idx = t.get_device()                                # -1 on the CPU
+    if idx < 0:
         raise ValueError(f"{name} must be a CUDA tensor")
-    if device is not None and t.device != device:
-        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if device is not None:
+        want = device if isinstance(device, int) else device.index
+        if idx != want:
+            raise ValueError(f"{name} is on cuda:{idx}, expected cuda:{want}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if ndim is not None and t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+
+
+class _on_device:
+    """Makes CUDA device `idx` current for the call (a no-op when it already
+    is, which is the common case)."""
+
+    __slots__ = ("idx", "prev")
+
+    def __init__(self, idx):
+        self.idx = idx if isinstance(idx, int) else idx.index
+        self.prev = None
+
+    def __enter__(self):
+        cur = torch.cuda.current_device()
+        if cur != self.idx:
+            self.prev = cur
+            torch.cuda.set_device(self.idx)
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            torch.cuda.set_device(self.prev)
 
 
 def version() -> int:
@@ -148,7 +174,7 @@ def paged_kv_write(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None) ->
     """k_cache/v_cache bf16 [NB, bs, Hkv, D] (in place) <- k_new/v_new bf16
     [T, Hkv, D] at rows slot_mapping int32 [T] (negative = skip)."""
     _need(k_cache, "k_cache", torch.bfloat16, 4)
-    dev = k_cache.device
+    dev = k_cache.get_device()
     _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
     _need(k_new, "k_new", torch.bfloat16, 3, dev)
     _need(v_new, "v_new", torch.bfloat16, 3, dev)
@@ -159,7 +185,7 @@ def paged_kv_write(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None) ->
     t = slot_mapping.shape[0]
     if k_new.shape != (t, hkv, d) or v_new.shape != (t, hkv, d):
         raise ValueError(f"k_new/v_new must be [{t}, {hkv}, {d}]")
-    with torch.cuda.device(dev):
+    with _on_device(dev):
         _check(_load().tvl_paged_kv_write(_ptr(k_new), _ptr(v_new), _ptr(k_cache),
                                           _ptr(v_cache), _ptr(slot_mapping), t, hkv, d, bs, nb,
                                           _stream(stream)))
@@ -170,7 +196,7 @@ def rope_paged_kv_write(q, k_new, v_new, k_cache, v_cache, slot_mapping, positio
     """RoPE of q (in place; may be None) and of k_new at `positions` (int32
     [T]), then the paged write of the rotated K rows and the V rows."""
     _need(k_cache, "k_cache", torch.bfloat16, 4)
-    dev = k_cache.device
+    dev = k_cache.get_device()
     _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
     _need(k_new, "k_new", torch.bfloat16, 3, dev)
     _need(v_new, "v_new", torch.bfloat16, 3, dev)
@@ -186,7 +212,7 @@ def rope_paged_kv_write(q, k_new, v_new, k_cache, v_cache, slot_mapping, positio
         hq = q.shape[1]
     if k_new.shape != (t, hkv, d) or v_new.shape != (t, hkv, d) or positions.shape[0] != t:
         raise ValueError("k_new/v_new must be [T, Hkv, D] and positions [T]")
-    with torch.cuda.device(dev):
+    with _on_device(dev):
         _check(_load().tvl_rope_paged_kv_write(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
                                                _ptr(v_cache), _ptr(slot_mapping),
                                                _ptr(positions), t, hq, hkv, d, bs, nb,
@@ -196,11 +222,22 @@ def rope_paged_kv_write(q, k_new, v_new, k_cache, v_cache, slot_mapping, positio
 def paged_attention_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                           max_blocks_per_seq, block_size,
                                           partition_size=0) -> int:
+    """Bytes of workspace the decode needs (tvl_paged_attention_decode_workspace_size)
+    on the current device; the answer is remembered per device and shape."""
+    key = (torch.cuda.current_device() if torch.cuda.is_available() else -1, num_seqs,
+           num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size, partition_size)
+    hit = _ws_sizes.get(key)
+    if hit is not None:
+        return hit
     out = ctypes.c_size_t(0)
     _check(_load().tvl_paged_attention_decode_workspace_size(
         num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size,
         partition_size, ctypes.byref(out)))
+    _ws_sizes[key] = int(out.value)
     return int(out.value)
+
+
+_ws_sizes = {}
 
 
 def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
@@ -208,7 +245,7 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
     """out fp32 [S, Hq, D] <- paged decode attention of q bf16 [S, Hq, D].
     workspace: uint8 CUDA tensor (allocated here when None and needed)."""
     _need(k_cache, "k_cache", torch.bfloat16, 4)
-    dev = k_cache.device
+    dev = k_cache.get_device()
     _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
     _need(q, "q", torch.bfloat16, 3, dev)
     _need(out, "out", torch.float32, 3, dev)
@@ -221,7 +258,7 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
     if block_tables.shape[0] != s or context_lens.shape[0] != s:
         raise ValueError("block_tables / context_lens must have num_seqs rows")
     mb = block_tables.shape[1]
-    with torch.cuda.device(dev):
+    with _on_device(dev):
         need = paged_attention_decode_workspace_size(s, hq, hkv, d, mb, bs, partition_size)
         if workspace is None and need > 0:
             workspace = torch.empty(need, dtype=torch.uint8, device=dev)
@@ -242,7 +279,7 @@ def paged_decode_step(out, q, k_new, v_new, k_cache, v_cache, block_tables, cont
     out fp32 [S, Hq, D] <- paged decode attention of q bf16 [S, Hq, D] over
     the updated cache."""
     _need(k_cache, "k_cache", torch.bfloat16, 4)
-    dev = k_cache.device
+    dev = k_cache.get_device()
     _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
     _need(q, "q", torch.bfloat16, 3, dev)
     _need(k_new, "k_new", torch.bfloat16, 3, dev)
@@ -259,7 +296,7 @@ def paged_decode_step(out, q, k_new, v_new, k_cache, v_cache, block_tables, cont
     if block_tables.shape[0] != s or context_lens.shape[0] != s:
         raise ValueError("block_tables / context_lens must have num_seqs rows")
     mb = block_tables.shape[1]
-    with torch.cuda.device(dev):
+    with _on_device(dev):
         need = paged_attention_decode_workspace_size(s, hq, hkv, d, mb, bs, partition_size)
         if workspace is None and need > 0:
             workspace = torch.empty(need, dtype=torch.uint8, device=dev)
@@ -278,7 +315,7 @@ def paged_attention_prefill(out, q, query_start_loc, k_cache, v_cache, block_tab
     """out fp32 [Tq, Hq, D] <- causal attention of the last Lq tokens of each
     sequence (q bf16 [Tq, Hq, D], packed by query_start_loc int32 [S+1])."""
     _need(k_cache, "k_cache", torch.bfloat16, 4)
-    dev = k_cache.device
+    dev = k_cache.get_device()
     _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
     _need(q, "q", torch.bfloat16, 3, dev)
     _need(out, "out", torch.float32, 3, dev)
@@ -293,7 +330,7 @@ def paged_attention_prefill(out, q, query_start_loc, k_cache, v_cache, block_tab
     if query_start_loc.shape[0] != s + 1 or block_tables.shape[0] != s:
         raise ValueError("query_start_loc must be [S+1] and block_tables [S, MB]")
     mb = block_tables.shape[1]
-    with torch.cuda.device(dev):
+    with _on_device(dev):
         _check(_load().tvl_paged_attention_prefill(
             _ptr(out), _ptr(q), _ptr(query_start_loc), _ptr(k_cache), _ptr(v_cache),
             _ptr(block_tables), _ptr(context_lens), s, tq, int(max_q_len), hq, hkv, d, bs, nb,
@@ -321,14 +358,14 @@ def copy_blocks(k_cache, v_cache, src, dst, stream=None) -> None:
     """Physical block dst[i] of both caches <- block src[i] (int32 CUDA
     tensors [n]); bit-exact; the pairs must not overlap."""
     _need(k_cache, "k_cache", torch.bfloat16, 4)
-    dev = k_cache.device
+    dev = k_cache.get_device()
     _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
     _need(src, "src", torch.int32, 1, dev)
     _need(dst, "dst", torch.int32, 1, dev)
     if src.shape != dst.shape:
         raise ValueError("src and dst differ in length")
     nb, bs, hkv, d = k_cache.shape
-    with torch.cuda.device(dev):
+    with _on_device(dev):
         _check(_load().tvl_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(src), _ptr(dst),
                                        src.numel(), hkv, d, bs, nb, _stream(stream)))
 

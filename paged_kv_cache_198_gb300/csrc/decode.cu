@@ -18,7 +18,15 @@
 //     one CTA each.
 // A segment that covers its whole sequence writes the final output; any other
 // writes a partial (m, l, acc) record, and merge_kernel combines the records
-// of a sequence by log-sum-exp -- the associative form of the online softmax.
+// of a sequence by log-sum-exp -- the associative form of the online softmax
+// (loads of 16 records in flight at once, the batch maximum moving the
+// running one; four warps per head when a sequence has many records).
+//
+// Decode step (tvl_paged_decode_step): the producer of the CTA that streams a
+// sequence's last block also writes the step's new token into the cache --
+// it loads the new K/V rows when the segment starts and stores them into row
+// (ctx - 1) % bs of that block, with a proxy fence, before it issues the
+// block's bulk copy -- so the write needs no kernel of its own.
 //
 // CTA structure.  One producer warp walks the CTA's segments and, per stage
 // of 32 tokens (two physical blocks of 16 or one of 32), issues 1-D bulk
@@ -961,9 +969,14 @@ __global__ void __launch_bounds__(kMergeHeads * kMergeMaxParts * 32)
 template <int G, int BS>
 cudaError_t launch_t(const Params& prm, dim3 grid, uint32_t smem_bytes, cudaStream_t stream) {
   auto kern = decode_kernel<G, BS>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  // the shared-memory limit, once per device: the opt-in maximum of a block
+  constexpr int kMaxDynSmem = 227 * 1024;
+  static PerDeviceOnce once;
+  cudaError_t e = once.run([&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+  });
   if (e != cudaSuccess) return e;
+  if (smem_bytes > static_cast<uint32_t>(kMaxDynSmem)) return cudaErrorInvalidConfiguration;
   return launch_pdl(kern, grid, dim3((prm.hpc + 1) * 32), smem_bytes, stream, prm);
 }
 

@@ -2,11 +2,30 @@
 // translation units.  Arguments arrive here already validated.
 #pragma once
 
+#include <atomic>
+
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
 
 namespace tvl {
+
+// Runs a set-up step (e.g. a kernel attribute) once per device: the first
+// successful run on a device is remembered, later calls on it return at once.
+struct PerDeviceOnce {
+  std::atomic<unsigned long long> done{0};   // bit d: device d set up
+  template <typename F>
+  cudaError_t run(F&& set_up) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = set_up();
+    if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+  }
+};
 
 struct KvWriteArgs {
   const void* k_new;

@@ -555,18 +555,24 @@ template <int NH>
 cudaError_t launch_nh(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                       const Params& p, int num_seqs, cudaStream_t stream) {
   using C = Cfg<NH>;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<NH>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-  if (e != cudaSuccess) return e;
-  if (NH == 2) {
+  // once per device: the shared-memory limit, and the check that the
+  // register split fits the registers the block is launched with
+  static PerDeviceOnce once;
+  cudaError_t e = once.run([] {
+    cudaError_t r = cudaFuncSetAttribute(prefill_kernel<NH>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (r != cudaSuccess || NH != 2) return r;
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, prefill_kernel<NH>);
-    if (e != cudaSuccess) return e;
+    r = cudaFuncGetAttributes(&fa, prefill_kernel<NH>);
+    if (r != cudaSuccess) return r;
     if (fa.numRegs * C::kThreads < 2 * 128 * kRegsSoftmax + 128 * kRegsAux) {
       set_last_error("prefill kernel register allocation smaller than its register split");
       return cudaErrorInvalidConfiguration;
     }
-  }
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
   dim3 grid(p.n_qtiles, p.hq / NH, num_seqs);
   return launch_pdl(prefill_kernel<NH>, grid, dim3(C::kThreads), C::kSmemBytes, stream, tq, tk,
                     tv, p);
