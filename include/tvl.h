@@ -161,7 +161,7 @@ tvl_status tvl_paged_attention_decode_workspace_size(
  * workspace: device memory of at least the size reported by
  *   tvl_paged_attention_decode_workspace_size (may be NULL when that is 0);
  *   its contents on entry are ignored and on exit unspecified.
- * Supported: D == 64, G in {1, 2, 4, 8}, bs in {16, 32}, Hkv <= 8 or a
+ * Supported: D == 64, G in {1, 2, 4, 8}, bs in {16, 32, 64, 128}, Hkv <= 8 or a
  * multiple of 8 (for G == 8: Hkv <= 4 or a multiple of 4).
  */
 tvl_status tvl_paged_attention_decode(

@@ -96,7 +96,8 @@ tvl_status decode_sizes(int num_seqs, int hq, int hkv, int d, int mb, int bs, in
                         long long* records, int* part_blocks, int* max_splits, int* ctas) {
   if (num_seqs < 0) return fail(TVL_ERR_INVALID_ARG, "num_seqs %d < 0", num_seqs);
   if (mb <= 0) return fail(TVL_ERR_INVALID_ARG, "max_blocks_per_seq %d <= 0", mb);
-  if (bs != 16 && bs != 32) return fail(TVL_ERR_UNSUPPORTED, "block_size %d (decode: 16, 32)", bs);
+  if (bs != 16 && bs != 32 && bs != 64 && bs != 128)
+    return fail(TVL_ERR_UNSUPPORTED, "block_size %d (decode: 16, 32, 64, 128)", bs);
   if (part < 0 || part % bs != 0)
     return fail(TVL_ERR_INVALID_ARG, "partition_size %d not a non-negative multiple of %d", part,
                 bs);

@@ -202,7 +202,7 @@ __device__ void producer(const Params& p, const Schedule& sc, uint8_t* smem, con
   const int hg = blockIdx.z;
   const int hpc = p.hpc;
   const bool whole_rows = (hpc == p.hkv);
-  constexpr int BPS = kStageTokens / BS;               // physical blocks per stage
+  constexpr int BPS = BS <= kStageTokens ? kStageTokens / BS : 1;   // blocks per stage
   const uint32_t blk_bytes = BS * hpc * kRowBytes;     // one block, the CTA's heads
   const uint32_t kv_bytes = kStageTokens * hpc * kRowBytes;
   const uint32_t q_bytes = hpc * G * kRowBytes;
@@ -267,6 +267,87 @@ __device__ void producer(const Params& p, const Schedule& sc, uint8_t* smem, con
         }
       }
     }
+    if constexpr (BS > kStageTokens) {
+      // Blocks larger than a stage: each block is streamed as BS / 32 stages
+      // of 32 tokens (the last block only as far as the context reaches).
+      constexpr int kSubPerBlock = BS / kStageTokens;
+      for (long long blk = b; blk < e && ok; ++blk) {
+        const int slot = static_cast<int>((blk - b) & 31);
+        if (slot == 0) tbl = (blk + lane < e) ? table[blk + lane] : 0;
+        int phys = __shfl_sync(kFull, tbl, slot);
+        bool phys_ok = true;
+        if (phys < 0 || phys >= p.num_blocks) {
+          if (lane == 0) report(p.status, TVL_DEV_BAD_BLOCK_ID);
+          phys = 0;
+          phys_ok = false;
+        }
+        const long long tok0 = blk * BS;                // first token of the block
+        const int nsub = blk == nb - 1
+                             ? static_cast<int>((ctx - tok0 + kStageTokens - 1) / kStageTokens)
+                             : kSubPerBlock;
+        for (int sub = 0; sub < nsub && ok; ++sub) {
+          int st;
+          if (!acquire(st)) {
+            ok = false;
+            break;
+          }
+          const int t0 = sub * kStageTokens;            // first token of the stage in the block
+          const bool first = (blk == b && sub == 0);
+          const bool last_stage = (blk == e - 1 && sub == nsub - 1);
+          uint8_t* kdst = smem + static_cast<size_t>(st) * p.stage_bytes;
+          uint8_t* vdst = kdst + kv_bytes;
+          uint8_t* qdst = vdst + kv_bytes;
+          if (lane == 0) {
+            StageMeta m;
+            m.seq = s;
+            const long long rem = ctx - tok0 - t0;
+            m.valid = static_cast<int>(rem < kStageTokens ? rem : kStageTokens);
+            m.flags = (first ? kSegFirst : 0) | (last_stage ? kSegLast : 0);
+            m.record = record;
+            meta[st] = m;
+            mbar_arrive_expect_tx(&full[st], 2 * kv_bytes + (first ? q_bytes : 0));
+          }
+          if (fused_write && blk == nb - 1 && phys_ok &&
+              sub == static_cast<int>((ctx - 1 - tok0) / kStageTokens)) {
+            // the new token's rows, stored before this stage's copy reads them
+            const size_t row =
+                ((static_cast<size_t>(phys) * BS + (ctx - 1 - tok0)) * p.hkv + hg * hpc) * kD;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const int c = lane + 32 * i;
+              if (c < wchunks) {
+                reinterpret_cast<uint4*>(p.k_cache_w + row)[c] = wk[i];
+                reinterpret_cast<uint4*>(p.v_cache_w + row)[c] = wv[i];
+              }
+            }
+            asm volatile("fence.proxy.async;" ::: "memory");
+            __syncwarp();
+            asm volatile("fence.proxy.async;" ::: "memory");
+          }
+          __syncwarp();
+          if (whole_rows) {
+            if (lane == 0) {                            // 32 contiguous token rows
+              const size_t off = (static_cast<size_t>(phys) * BS + t0) * p.hkv * kD;
+              bulk_load(kdst, p.k_cache + off, kv_bytes, &full[st], stream_policy);
+              bulk_load(vdst, p.v_cache + off, kv_bytes, &full[st], stream_policy);
+            }
+          } else {
+            const int t = lane;                         // one token row per lane
+            const size_t off =
+                ((static_cast<size_t>(phys) * BS + t0 + t) * p.hkv + hg * hpc) * kD;
+            bulk_load(kdst + t * hpc * kRowBytes, p.k_cache + off, hpc * kRowBytes, &full[st],
+                      stream_policy);
+            bulk_load(vdst + t * hpc * kRowBytes, p.v_cache + off, hpc * kRowBytes, &full[st],
+                      stream_policy);
+          }
+          if (first && lane == 31) {
+            const size_t off = (static_cast<size_t>(s) * p.hq + hg * hpc * G) * kD;
+            bulk_load(qdst, p.q + off, q_bytes, &full[st], keep_policy);
+          }
+          ++it;
+        }
+      }
+    } else
     for (long long blk = b; blk < e && ok; blk += BPS) {
       const int slot = static_cast<int>((blk - b) & 31);   // BPS divides 32
       if (slot == 0) tbl = (blk + lane < e) ? table[blk + lane] : 0;
@@ -1057,15 +1138,23 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     grid = dim3(a.balanced_ctas, 1, groups);
 
   cudaError_t e = cudaErrorInvalidValue;
-  switch (G * 100 + bs) {
-    case 116: e = launch_t<1, 16>(prm, grid, smem, stream); break;
-    case 132: e = launch_t<1, 32>(prm, grid, smem, stream); break;
-    case 216: e = launch_t<2, 16>(prm, grid, smem, stream); break;
-    case 232: e = launch_t<2, 32>(prm, grid, smem, stream); break;
-    case 416: e = launch_t<4, 16>(prm, grid, smem, stream); break;
-    case 432: e = launch_t<4, 32>(prm, grid, smem, stream); break;
-    case 816: e = launch_t<8, 16>(prm, grid, smem, stream); break;
-    case 832: e = launch_t<8, 32>(prm, grid, smem, stream); break;
+  switch (G * 1000 + bs) {
+    case 1016: e = launch_t<1, 16>(prm, grid, smem, stream); break;
+    case 1032: e = launch_t<1, 32>(prm, grid, smem, stream); break;
+    case 1064: e = launch_t<1, 64>(prm, grid, smem, stream); break;
+    case 1128: e = launch_t<1, 128>(prm, grid, smem, stream); break;
+    case 2016: e = launch_t<2, 16>(prm, grid, smem, stream); break;
+    case 2032: e = launch_t<2, 32>(prm, grid, smem, stream); break;
+    case 2064: e = launch_t<2, 64>(prm, grid, smem, stream); break;
+    case 2128: e = launch_t<2, 128>(prm, grid, smem, stream); break;
+    case 4016: e = launch_t<4, 16>(prm, grid, smem, stream); break;
+    case 4032: e = launch_t<4, 32>(prm, grid, smem, stream); break;
+    case 4064: e = launch_t<4, 64>(prm, grid, smem, stream); break;
+    case 4128: e = launch_t<4, 128>(prm, grid, smem, stream); break;
+    case 8016: e = launch_t<8, 16>(prm, grid, smem, stream); break;
+    case 8032: e = launch_t<8, 32>(prm, grid, smem, stream); break;
+    case 8064: e = launch_t<8, 64>(prm, grid, smem, stream); break;
+    case 8128: e = launch_t<8, 128>(prm, grid, smem, stream); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;

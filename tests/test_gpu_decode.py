@@ -103,6 +103,9 @@ CASES = [
     ([700, 250, 1], 32, 4, 16),            # G = 8
     ([77, 513, 2049], 32, 16, 16),         # 16 KV heads: two KV-head groups
     ([0, 40, 0, 9], 8, 2, 32),             # empty contexts give zeros
+    ([1, 63, 64, 65, 700, 2048], 32, 8, 64),   # blocks of 64: two stages each
+    ([1, 127, 128, 129, 900], 16, 4, 128),     # blocks of 128: four stages each
+    ([300, 5, 1500], 64, 8, 128),              # G = 8 (two KV-head groups), blocks of 128
 ]
 
 
@@ -110,6 +113,8 @@ CASES = [
 @pytest.mark.parametrize("part", [0, 32, 256])
 def test_decode_random_shapes(case, part):
     ctx, hq, hkv, bs = CASES[case]
+    if part % bs:
+        part = bs                   # windows must be whole blocks: one block each
     wl = W.make_decode(500 + case, ctx, num_q_heads=hq, num_kv_heads=hkv, block_size=bs)
     got, _ = gpu_decode(wl, partition_size=part)
     ref = oracle_decode(wl)

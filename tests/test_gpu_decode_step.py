@@ -37,6 +37,8 @@ CASES = [
     ([900, 5, 1024, 2500], 64, 8, 16, 0),       # G = 8: two KV-head groups per sequence
     ([129, 7, 3000], 8, 8, 16, 0),              # G = 1
     ([129, 7, 3000, 0, 44], 16, 8, 32, 512),    # G = 2, an empty sequence
+    ([1, 64, 65, 700, 2047], 32, 8, 64, 0),     # blocks of 64
+    ([128, 129, 5, 1000], 64, 8, 128, 256),     # G = 8, blocks of 128, fixed windows
 ]
 
 

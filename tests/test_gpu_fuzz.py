@@ -40,9 +40,9 @@ def _ctx_list(rng, n, cap):
 def test_fuzz_decode_and_step(seed):
     rng = random.Random(9000 + seed)
     hq, hkv = rng.choice(GROUPS)
-    bs = rng.choice([16, 32])
+    bs = rng.choice([16, 32, 16, 32, 64, 128])
     ctx = _ctx_list(rng, rng.randint(1, 40), rng.choice([64, 700, 3000]))
-    part = rng.choice([0, 0, bs, 4 * bs, 256 // bs * bs, 1024])
+    part = rng.choice([0, 0, bs, 4 * bs, max(bs, 256 // bs * bs), 1024])
     wl = W.make_decode(9100 + seed, ctx, num_q_heads=hq, num_kv_heads=hkv, block_size=bs)
     t = W.to_device(wl, DEV)
     s, _, d = wl.q.shape
