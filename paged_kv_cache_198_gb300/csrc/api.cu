@@ -5,6 +5,7 @@
 // CUDA API reports errors through return values, which must not be ignored].
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -405,6 +406,8 @@ tvl_status tvl_paged_attention_prefill(float* out, const void* q, const int32_t*
   if (num_seqs == 0 || total_q_tokens == 0) return TVL_OK;
   if (max_q_len == 0) return fail(TVL_ERR_INVALID_ARG, "max_q_len 0 with queries present");
   if (num_seqs > 65535) return fail(TVL_ERR_UNSUPPORTED, "num_seqs %d > 65535", num_seqs);
+  if (static_cast<long long>(num_seqs) * ((max_q_len + 127) / 128) * num_q_heads > INT_MAX)
+    return fail(TVL_ERR_UNSUPPORTED, "num_seqs * ceil(max_q_len / 128) * num_q_heads > 2^31 - 1");
   if (!out || !q || !query_start_loc || !k_cache || !v_cache || !block_tables || !context_lens)
     return fail(TVL_ERR_INVALID_ARG, "null pointer argument");
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))

@@ -75,7 +75,8 @@ struct Cfg {
   static constexpr uint32_t kKOff = NH * kTileBytes;
   static constexpr uint32_t kVOff = kKOff + kStages * kTileBytes;
   static constexpr uint32_t kBarOff = kVOff + kStages * kTileBytes;
-  static constexpr uint32_t kSmemBytes = kBarOff + 512 + 1024;   // + 1 KB alignment slack
+  static constexpr uint32_t kOrderOff = kBarOff + 512;            // item keys + the chosen item
+  static constexpr uint32_t kSmemBytes = kOrderOff + 4 * (kThreads + 1) + 1024;   // + alignment slack
   static constexpr uint32_t kTmemCols = NH == 2 ? 512 : 256;
   __device__ static uint32_t s_col(int h) { return h * kBN; }
   __device__ static uint32_t o_col(int h) { return NH * kBN + h * kD; }
@@ -164,15 +165,51 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Barriers* B = reinterpret_cast<Barriers*>(smem + C::kBarOff);
 
-  const int qtile = p.n_qtiles - 1 - static_cast<int>(blockIdx.x);   // longest tiles first
-  const int h0 = blockIdx.y * NH;                                     // first query head
-  const int s = blockIdx.z;
+  const int pairs = p.hq / NH;                                        // head groups per item
+  const int h0 = static_cast<int>(blockIdx.x % pairs) * NH;           // first query head
   const int g = h0 / p.group;                                         // shared KV head
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   grid_dependency_wait();          // inputs may come from the preceding kernel
   grid_dependents_launch();
+
+  // ---- which (sequence, query tile) item this CTA takes.  Item i is
+  // sequence i / n_qtiles, query tile n_qtiles - 1 - i % n_qtiles.  CTAs
+  // start in index order, so the CTAs with the lowest indices get the items
+  // with the most key tiles (ties in item order): the long items do not
+  // land in the last wave.  Every CTA ranks the items the same way from the
+  // lengths (one item per thread: beyond that, item order is kept).  The
+  // ranks are a permutation of the items whatever the lengths hold.
+  const int n_items = p.num_seqs * p.n_qtiles;
+  int item = static_cast<int>(blockIdx.x / pairs);
+  if (n_items <= C::kThreads) {
+    int* keys = reinterpret_cast<int*>(smem + C::kOrderOff);
+    const int i = threadIdx.x;
+    int key = 0;
+    if (i < n_items) {
+      const int si = i / p.n_qtiles;
+      const int qt = p.n_qtiles - 1 - i % p.n_qtiles;
+      const int lqi = p.query_start_loc[si + 1] - p.query_start_loc[si];
+      const int last = p.context_lens[si] - lqi + min((qt + 1) * kBM, lqi);   // keys seen
+      key = qt * kBM >= lqi ? 0 : (last + kBN - 1) / kBN;
+      keys[i] = key;
+    }
+    __syncthreads();
+    if (i < n_items) {
+      int r = 0;
+      for (int j = 0; j < n_items; ++j) {
+        const int kj = keys[j];
+        r += (kj > key || (kj == key && j < i)) ? 1 : 0;
+      }
+      if (r == item) keys[C::kThreads] = i;
+    }
+    __syncthreads();
+    item = keys[C::kThreads];
+  }
+  item = __shfl_sync(kFull, item, 0);   // warp-uniform to the compiler (0 spills)
+  const int s = item / p.n_qtiles;
+  const int qtile = p.n_qtiles - 1 - item % p.n_qtiles;
 
   // ---- per-tile geometry (identical in every thread)
   const int q0 = p.query_start_loc[s];
@@ -573,7 +610,7 @@ cudaError_t launch_nh(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
     return cudaSuccess;
   });
   if (e != cudaSuccess) return e;
-  dim3 grid(p.n_qtiles, p.hq / NH, num_seqs);
+  dim3 grid(static_cast<unsigned>(num_seqs) * p.n_qtiles * (p.hq / NH));
   return launch_pdl(prefill_kernel<NH>, grid, dim3(C::kThreads), C::kSmemBytes, stream, tq, tk,
                     tv, p);
 }

@@ -52,6 +52,21 @@ def test_prefill_random_shapes(case):
     assert_clean_status()
 
 
+@pytest.mark.parametrize("hkv", [2, 8])    # two query heads per CTA / one
+def test_prefill_more_items_than_threads(hkv):
+    """400 (sequence, query tile) items: more than a CTA has threads, so the
+    CTAs take the items in item order instead of longest first.  Every row of
+    every sequence is still written once (the output starts as NaN)."""
+    gen = np.random.default_rng(31)
+    lq = gen.integers(1, 40, 200).tolist()
+    lq[7] = 200                                  # two query tiles for every sequence
+    prefix = gen.integers(0, 300, 200).tolist()
+    wl = W.make_prefill(731, prefix, lq, num_q_heads=8, num_kv_heads=hkv, block_size=16)
+    got, _ = gpu_prefill(wl)
+    assert_close(got, oracle_prefill(wl), f"400 items hkv {hkv}")
+    assert_clean_status()
+
+
 @pytest.mark.parametrize("replica", [0, 1, 2])
 def test_prefill_chunked_config_sampled(replica):
     wl = W.named("chunked_prefill", replica)
