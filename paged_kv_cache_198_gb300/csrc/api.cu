@@ -434,6 +434,8 @@ tvl_status tvl_paged_attention_prefill(float* out, const void* q, const int32_t*
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.scale = scale;
   a.status = word;
+  st = sm_count(&a.num_sms);
+  if (st != TVL_OK) return st;
   cudaError_t e = tvl::launch_prefill(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return TVL_OK;

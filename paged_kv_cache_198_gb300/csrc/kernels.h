@@ -120,6 +120,7 @@ struct PrefillArgs {
   int block_size, num_blocks, max_blocks_per_seq;
   float scale;
   uint32_t* status;
+  int num_sms;            // the persistent grid's size bound
 };
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 

@@ -8,9 +8,13 @@
 // the Lq new query tokens of a sequence are its last Lq positions; row i at
 // absolute position p = ctx - Lq + i attends to cached tokens 0..p.
 //
-// One CTA = one 128-row query tile of NH query heads of the same GQA group
-// (NH = 2 when the group has two or more heads), so each K/V tile gathered
-// from the paged cache serves NH heads.  Warps:
+// A unit of work is one 128-row query tile of NH query heads of the same GQA
+// group (NH = 2 when the group has two or more heads), so each K/V tile
+// gathered from the paged cache serves NH heads.  The kernel is persistent:
+// one CTA per SM walks its share of the units (longest first, dealt in snake
+// order), and the K/V ring, the barriers and TMEM carry on from one unit to
+// the next, so a unit's loads and first Q K^T overlap the previous unit's
+// last softmax and its output.  Warps:
 //   0..4NH-1  softmax, one warpgroup per head: thread r owns query row r
 //             (TMEM lane r).  Per 128-key tile it loads its 128 scores into
 //             registers and releases S at once, so the next tile's Q K^T
@@ -21,8 +25,9 @@
 //             and recompute P from the scores still in registers (O in TMEM
 //             is then rescaled; exact, since one reference scales numerator
 //             and denominator).  P is stored as fp16 into TMEM once the
-//             previous P.V has consumed the buffer.  At the end it
-//             normalises O and writes it out;
+//             previous P.V has consumed the buffer.  At a unit's end it
+//             normalises O and sends each row out of a staging row in
+//             shared memory with one bulk copy;
 //   4NH       producer: TMA loads of the Q tiles and, per 128-key tile, one
 //             box of bs tokens x 64 dims per physical block (K and V) found
 //             through the block table -- the paged gather; blocks past the
@@ -31,8 +36,8 @@
 //             shared memory) and O_h += P_h V (M 128, N 64, fp16, P read from
 //             TMEM, V an MN-major shared operand), fp32 accumulation.  The
 //             next tile's S is issued as soon as the softmax has released S,
-//             before this tile's P.V.  Completion is signalled by
-//             tcgen05.commit;
+//             before this tile's P.V (on a unit's last tile, after it).
+//             Completion is signalled by tcgen05.commit;
 //   4NH+2,+3  V conversion: each V tile bf16 -> fp16 in place (exact for
 //             |v| >= 2^-14; keys past the context become 0).
 // P and V go through fp16 rather than bf16 so that rounding P costs at most
@@ -56,7 +61,9 @@ namespace {
 constexpr int kD = 64;
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-constexpr int kStages = 5;
+constexpr int kStages = 3;
+constexpr int kOPitch = kD * 4 + 16;    // bytes per staged output row: 16-byte rows
+                                        // land on distinct banks (no conflicts)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr uint32_t kTileBytes = kBM * kD * 2;      // 16 KB: 128 rows x 128 B
@@ -74,10 +81,12 @@ struct Cfg {
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKOff = NH * kTileBytes;
   static constexpr uint32_t kVOff = kKOff + kStages * kTileBytes;
-  static constexpr uint32_t kBarOff = kVOff + kStages * kTileBytes;
-  static constexpr uint32_t kOrderOff = kBarOff + 512;            // item keys + the chosen item
-  static constexpr uint32_t kSmemBytes = kOrderOff + 4 * (kThreads + 1) + 1024;   // + alignment slack
+  static constexpr uint32_t kStageOff = kVOff + kStages * kTileBytes;   // output rows
+  static constexpr uint32_t kBarOff = kStageOff + NH * kBM * kOPitch;
+  static constexpr uint32_t kTabOff = kBarOff + 512;    // item order, lengths, rank keys
+  static constexpr uint32_t kSmemBytes = kTabOff + 5 * 4 * kThreads + 1024;   // + alignment slack
   static constexpr uint32_t kTmemCols = NH == 2 ? 512 : 256;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per block");
   __device__ static uint32_t s_col(int h) { return h * kBN; }
   __device__ static uint32_t o_col(int h) { return NH * kBN + h * kD; }
   __device__ static uint32_t p_col(int h) { return NH * (kBN + kD) + h * (kBN / 2); }
@@ -85,14 +94,15 @@ struct Cfg {
 
 // Register split of the two-head kernel: 12 warps launched with 168
 // registers each (64512); the producer / MMA / conversion warpgroup drops to
-// 64 and the two softmax warpgroups rise to 216, which holds a row's 128
-// scores and its 64 packed P together: 2 x 128 x 216 + 128 x 64 = 63488.
+// 72 and the two softmax warpgroups rise to 216, which holds a row's 128
+// scores and its 64 packed P together: 2 x 128 x 216 + 128 x 72 = 64512.
 // The host checks the launch allocation before the first launch.
 constexpr int kRegsSoftmax = 216;
-constexpr int kRegsAux = 64;
+constexpr int kRegsAux = 72;
 
 struct Barriers {
   uint64_t q_full;
+  uint64_t q_empty;
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t v_ready[kStages];
@@ -154,46 +164,129 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
   return false;
 }
 
+// One work unit: a 128-row query tile of NH query heads of one sequence.
+// Every role of the CTA derives the same units in the same order.
+struct Unit {
+  int s, h0, q0, row0, rows, pos_first, ctx, n_kv;
+  bool valid;      // rows to compute and consistent lengths
+  bool bad;        // rows but inconsistent lengths (reported, skipped)
+  bool bad_ctx;    // the inconsistency is a context past the table's capacity
+};
+
+// Index of the k-th unit of CTA c among G: the units in longest-first order
+// are dealt to the CTAs row by row, every other row reversed (c, 2G-1-c,
+// 2G+c, ...), which evens out the CTAs' totals.  Increases with k.
+__device__ __forceinline__ long long unit_index(int k, int c, int G) {
+  return static_cast<long long>(k) * G + ((k & 1) ? G - 1 - c : c);
+}
+
+
+// Unit u: rank u / pairs in the item order, head group u % pairs.  With
+// `tab`, the order and the items' lengths come from shared memory (tab[0..K)
+// rank -> item, then K-strided q0, Lq and context per item); without it the
+// order is the item order and the lengths are read from global memory.
+template <int NH, int K>
+__device__ __forceinline__ void unit_info(const Params& p, const int* tab, int u, Unit& x) {
+  const int pairs = p.hq / NH;
+  const int rank = u / pairs;
+  x.h0 = (u - rank * pairs) * NH;
+  int item, lq;
+  if (tab != nullptr) {
+    item = tab[rank];
+    x.q0 = tab[K + item];
+    lq = tab[2 * K + item];
+    x.ctx = tab[3 * K + item];
+  } else {
+    item = rank;
+    const int si = item / p.n_qtiles;
+    x.q0 = p.query_start_loc[si];
+    lq = p.query_start_loc[si + 1] - x.q0;
+    x.ctx = p.context_lens[si];
+  }
+  x.s = item / p.n_qtiles;
+  x.row0 = (p.n_qtiles - 1 - item % p.n_qtiles) * kBM;
+  const int cap = p.max_blocks * p.bs;
+  const bool rows_here = x.row0 < lq;
+  x.bad_ctx = x.ctx > cap;
+  x.bad = rows_here && (x.ctx < lq || x.bad_ctx);
+  x.valid = rows_here && !x.bad;
+  x.rows = min(kBM, lq - x.row0);
+  x.pos_first = x.ctx - lq + x.row0;
+  x.n_kv = (x.pos_first + x.rows - 1) / kBN + 1;
+}
+
+// The first unit of this CTA at or after index k that has work; k moves to
+// it.  With kWarp it is called by whole warps and the fields go through
+// lane 0, so that the compiler sees them warp-uniform (fewer registers).
+template <int NH, int K, bool kWarp>
+__device__ __forceinline__ bool next_valid_unit(const Params& p, const int* tab, int& k, Unit& x) {
+  const int n_units = p.num_seqs * p.n_qtiles * (p.hq / NH);
+  for (;; ++k) {
+    const long long u = unit_index(k, blockIdx.x, gridDim.x);
+    if (u >= n_units) return false;
+    unit_info<NH, K>(p, tab, static_cast<int>(u), x);
+    if (!kWarp) {
+      if (x.valid) return true;
+      continue;
+    }
+    if (__shfl_sync(kFull, x.valid ? 1 : 0, 0)) break;
+  }
+  x.s = __shfl_sync(kFull, x.s, 0);
+  x.h0 = __shfl_sync(kFull, x.h0, 0);
+  x.q0 = __shfl_sync(kFull, x.q0, 0);
+  x.row0 = __shfl_sync(kFull, x.row0, 0);
+  x.rows = __shfl_sync(kFull, x.rows, 0);
+  x.pos_first = __shfl_sync(kFull, x.pos_first, 0);
+  x.ctx = __shfl_sync(kFull, x.ctx, 0);
+  x.n_kv = __shfl_sync(kFull, x.n_kv, 0);
+  return true;
+}
+
 template <int NH>
 __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const Params p) {
   using C = Cfg<NH>;
+  constexpr int K = C::kThreads;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Barriers* B = reinterpret_cast<Barriers*>(smem + C::kBarOff);
-
-  const int pairs = p.hq / NH;                                        // head groups per item
-  const int h0 = static_cast<int>(blockIdx.x % pairs) * NH;           // first query head
-  const int g = h0 / p.group;                                         // shared KV head
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int G = static_cast<int>(gridDim.x);
+  const int c = static_cast<int>(blockIdx.x);
 
   grid_dependency_wait();          // inputs may come from the preceding kernel
   grid_dependents_launch();
 
-  // ---- which (sequence, query tile) item this CTA takes.  Item i is
-  // sequence i / n_qtiles, query tile n_qtiles - 1 - i % n_qtiles.  CTAs
-  // start in index order, so the CTAs with the lowest indices get the items
-  // with the most key tiles (ties in item order): the long items do not
-  // land in the last wave.  Every CTA ranks the items the same way from the
-  // lengths (one item per thread: beyond that, item order is kept).  The
-  // ranks are a permutation of the items whatever the lengths hold.
+  // ---- the item order.  Item i is sequence i / n_qtiles, query tile
+  // n_qtiles - 1 - i % n_qtiles.  Items with the most key tiles go first
+  // (ties in item order), so the long ones are not left for the end.  Every
+  // CTA ranks the items the same way from the lengths, one item per thread
+  // (beyond that, item order is kept); the ranks are a permutation of the
+  // items whatever the lengths hold.
+  const int n_units = p.num_seqs * p.n_qtiles * (p.hq / NH);   // < 2^31 (host check)
   const int n_items = p.num_seqs * p.n_qtiles;
-  int item = static_cast<int>(blockIdx.x / pairs);
-  if (n_items <= C::kThreads) {
-    int* keys = reinterpret_cast<int*>(smem + C::kOrderOff);
+  const int* tab = nullptr;
+  if (n_items <= K) {
+    int* t = reinterpret_cast<int*>(smem + C::kTabOff);
+    int* keys = t + 4 * K;
     const int i = threadIdx.x;
     int key = 0;
     if (i < n_items) {
       const int si = i / p.n_qtiles;
       const int qt = p.n_qtiles - 1 - i % p.n_qtiles;
-      const int lqi = p.query_start_loc[si + 1] - p.query_start_loc[si];
-      const int last = p.context_lens[si] - lqi + min((qt + 1) * kBM, lqi);   // keys seen
+      const int qa = p.query_start_loc[si];
+      const int lqi = p.query_start_loc[si + 1] - qa;
+      const int ci = p.context_lens[si];
+      const int last = ci - lqi + min((qt + 1) * kBM, lqi);   // keys seen
       key = qt * kBM >= lqi ? 0 : (last + kBN - 1) / kBN;
       keys[i] = key;
+      t[K + i] = qa;
+      t[2 * K + i] = lqi;
+      t[3 * K + i] = ci;
     }
     __syncthreads();
     if (i < n_items) {
@@ -202,37 +295,18 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
         const int kj = keys[j];
         r += (kj > key || (kj == key && j < i)) ? 1 : 0;
       }
-      if (r == item) keys[C::kThreads] = i;
+      t[r] = i;
     }
-    __syncthreads();
-    item = keys[C::kThreads];
+    tab = t;
   }
-  item = __shfl_sync(kFull, item, 0);   // warp-uniform to the compiler (0 spills)
-  const int s = item / p.n_qtiles;
-  const int qtile = p.n_qtiles - 1 - item % p.n_qtiles;
-
-  // ---- per-tile geometry (identical in every thread)
-  const int q0 = p.query_start_loc[s];
-  const int lq = p.query_start_loc[s + 1] - q0;
-  const int ctx = p.context_lens[s];
-  const int cap = p.max_blocks * p.bs;
-  if (qtile * kBM >= lq) return;                       // no rows here
-  if (ctx < lq || ctx > cap || lq < 0) {
-    if (threadIdx.x == 0)
-      report(p.status, ctx > cap ? TVL_DEV_BAD_CONTEXT_LEN : TVL_DEV_BAD_QUERY_LEN);
-    return;
-  }
-  const int prefix = ctx - lq;
-  const int row0 = qtile * kBM;                         // first row of the tile
-  const int rows = min(kBM, lq - row0);                 // valid rows
-  const int pos_first = prefix + row0;
-  const int pos_last = prefix + row0 + rows - 1;
-  const int n_kv = pos_last / kBN + 1;                  // KV tiles to visit
-  const int nblk = (ctx + p.bs - 1) / p.bs;
-  const int boxes = kBN / p.bs;                         // physical blocks per KV tile
+  const int* tab_or_null = n_items <= K ? reinterpret_cast<const int*>(smem + C::kTabOff) : nullptr;
+  auto next_unit = [&](int& k, Unit& x) -> bool {
+    return next_valid_unit<NH, K, true>(p, tab_or_null, k, x);
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(&B->q_full, 1);
+    mbar_init(&B->q_empty, 1);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&B->kv_full[i], 1);
       mbar_init(&B->kv_empty[i], 1);
@@ -261,58 +335,87 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
   if constexpr (NH == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsAux));
   if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ producer
+    // Per unit: the Q tiles once the previous unit's Q K^T MMAs are done
+    // (q_empty), then per 128-key tile one box of bs tokens x 64 dims per
+    // physical block (K and V) into the next stage of the ring.
     if (lane == 0) {
       prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);
-      mbar_arrive_expect_tx(&B->q_full, NH * kTileBytes);
-      for (int i = 0; i < NH; ++i)
-        tma_load_3d(smem + C::kQOff + i * kTileBytes, &tm_q, 0, h0 + i, q0 + row0, &B->q_full);
     }
-    const int32_t* table = p.block_tables + static_cast<long long>(s) * p.max_blocks;
-    for (int j = 0; j < n_kv; ++j) {
-      const int st = j % kStages;
-      bool ok = true;
-      if (j >= kStages && lane == 0)
-        ok = wait_or_abort(&B->kv_empty[st], ((j / kStages) - 1) & 1, B, p);
-      if (__shfl_sync(kFull, ok ? 1 : 0, 0) == 0) break;
-      if (lane == 0) mbar_arrive_expect_tx(&B->kv_full[st], 2 * kTileBytes);
-      __syncwarp();
-      for (int b = lane; b < boxes; b += 32) {
-        const int lb = j * boxes + b;                   // logical block
-        int phys = p.num_blocks;                        // out of range: zero fill
-        if (lb < nblk) {
-          phys = table[lb];
-          if (phys < 0 || phys >= p.num_blocks) {
-            report(p.status, TVL_DEV_BAD_BLOCK_ID);
-            phys = p.num_blocks;
-          }
+    const int boxes = kBN / p.bs;                       // physical blocks per KV tile
+    int gt = 0;                                         // KV tiles issued
+    int nq = 0;                                         // Q loads issued
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      Unit x;
+      if (!next_unit(k, x)) break;
+      if (lane == 0) {
+        if (nq > 0) ok = wait_or_abort(&B->q_empty, (nq - 1) & 1, B, p);
+        if (ok) {
+          mbar_arrive_expect_tx(&B->q_full, NH * kTileBytes);
+          for (int i = 0; i < NH; ++i)
+            tma_load_3d(smem + C::kQOff + i * kTileBytes, &tm_q, 0, x.h0 + i, x.q0 + x.row0,
+                        &B->q_full);
         }
-        const uint32_t off = static_cast<uint32_t>(b * p.bs) * (kD * 2);
-        tma_load_4d(smem + C::kKOff + st * kTileBytes + off, &tm_k, 0, g, 0, phys,
-                    &B->kv_full[st]);
-        tma_load_4d(smem + C::kVOff + st * kTileBytes + off, &tm_v, 0, g, 0, phys,
-                    &B->kv_full[st]);
+      }
+      ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      ++nq;
+      const int g = x.h0 / p.group;                     // shared KV head
+      const int nblk = (x.ctx + p.bs - 1) / p.bs;
+      const int32_t* table = p.block_tables + static_cast<long long>(x.s) * p.max_blocks;
+      for (int j = 0; j < x.n_kv; ++j, ++gt) {
+        const int st = gt % kStages;
+        if (gt >= kStages && lane == 0)
+          ok = wait_or_abort(&B->kv_empty[st], ((gt / kStages) - 1) & 1, B, p);
+        ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        if (lane == 0) mbar_arrive_expect_tx(&B->kv_full[st], 2 * kTileBytes);
+        __syncwarp();
+        for (int b = lane; b < boxes; b += 32) {
+          const int lb = j * boxes + b;                 // logical block
+          int phys = p.num_blocks;                      // out of range: zero fill
+          if (lb < nblk) {
+            phys = table[lb];
+            if (phys < 0 || phys >= p.num_blocks) {
+              report(p.status, TVL_DEV_BAD_BLOCK_ID);
+              phys = p.num_blocks;
+            }
+          }
+          const uint32_t off = static_cast<uint32_t>(b * p.bs) * (kD * 2);
+          tma_load_4d(smem + C::kKOff + st * kTileBytes + off, &tm_k, 0, g, 0, phys,
+                      &B->kv_full[st]);
+          tma_load_4d(smem + C::kVOff + st * kTileBytes + off, &tm_v, 0, g, 0, phys,
+                      &B->kv_full[st]);
+        }
       }
     }
     // the loads in flight must land before exit
     if (lane == 0) {
-      const int first = n_kv > kStages ? n_kv - kStages : 0;
-      for (int j = first; j < n_kv; ++j)
-        if (!mbar_wait(&B->kv_full[j % kStages], (j / kStages) & 1))
-          report(p.status, kDevTimeout);
-      if (!mbar_wait(&B->q_full, 0)) report(p.status, kDevTimeout);
+      for (int t = gt > kStages ? gt - kStages : 0; t < gt; ++t)
+        if (!mbar_wait(&B->kv_full[t % kStages], (t / kStages) & 1)) report(p.status, kDevTimeout);
+      if (nq > 0 && !mbar_wait(&B->q_full, (nq - 1) & 1)) report(p.status, kDevTimeout);
     }
   } else if (warp == C::kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    // Per key tile j and head h: S_h(j+1) = Q_h K(j+1)^T is issued as soon as
-    // the softmax has taken S_h(j) into registers (s_free), so it runs while
-    // P_h(j) is being computed; O_h += P_h(j) V(j) follows once P_h(j) is in
-    // TMEM (p_full) and V(j) is fp16 (v_ready).
+    // One stream of key tiles over all of the CTA's units.  For tile t and
+    // head h, S_h(t+1) = Q_h K(t+1)^T is issued as soon as the softmax has
+    // taken S_h(t) into registers (s_free) -- across a unit boundary too, so
+    // the next unit's first scores are computed during this unit's last
+    // softmax -- then O_h += P_h(t) V(t) once P_h(t) is in TMEM (p_full) and
+    // V(t) is fp16 (v_ready).  After a unit's last Q K^T, q_empty frees the
+    // Q buffer for the next unit.
+    // Lane 0 alone walks the units and issues: the tensor pipe queues
+    // little, so every cycle this thread spends outside tcgen05.mma (waits,
+    // bookkeeping) idles the pipe.
     if (lane == 0) {
+      auto next_unit1 = [&](int& k, Unit& x) -> bool {
+        return next_valid_unit<NH, K, false>(p, tab_or_null, k, x);
+      };
       const uint32_t q_addr = smem_addr(smem + C::kQOff);
-      auto issue_qk = [&](int j, int hh) {
-        const uint32_t k_addr = smem_addr(smem + C::kKOff + (j % kStages) * kTileBytes);
+      auto issue_qk = [&](int st, int hh) {
+        const uint32_t k_addr = smem_addr(smem + C::kKOff + st * kTileBytes);
         const uint32_t qa = q_addr + hh * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
@@ -320,35 +423,74 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
                      desc_sw128(k_addr + kk * 32, 16, 1024), kIdescQK, kk > 0);
         mma_commit(&B->s_full[hh]);
       };
-      bool ok = wait_or_abort(&B->q_full, 0, B, p) && wait_or_abort(&B->kv_full[0], 0, B, p);
+      int k = 0;
+      Unit cur;
+      bool ok = next_unit1(k, cur);
+      int gt = 0;                                       // tile whose P.V comes next
+      int nq = 0;                                       // index of cur among the units
       if (ok) {
-        tc_fence_after();
-        for (int hh = 0; hh < NH; ++hh) issue_qk(0, hh);
+        ok = wait_or_abort(&B->q_full, 0, B, p) && wait_or_abort(&B->kv_full[0], 0, B, p);
+        if (ok) {
+          tc_fence_after();
+          for (int hh = 0; hh < NH; ++hh) issue_qk(0, hh);
+          if (cur.n_kv == 1) mma_commit(&B->q_empty);
+        }
       }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j % kStages;
-        if (j + 1 < n_kv) {
-          ok = wait_or_abort(&B->kv_full[(j + 1) % kStages], ((j + 1) / kStages) & 1, B, p);
+      // stage and phase of tile gt (P.V next) and of tile gt + 1 (Q K^T next)
+      int st = 0, ph = 0;
+      int sn = kStages > 1 ? 1 : 0, phn = kStages > 1 ? 0 : 1;
+      while (ok) {
+        int kn = k + 1;
+        Unit nxt;
+        const bool has_nxt = next_unit1(kn, nxt);
+        for (int j = 0; ok && j < cur.n_kv; ++j, ++gt) {
+          // Within a unit the next S comes first, so the tensor pipe works
+          // while P is computed.  On a unit's last tile its P.V comes first:
+          // the next unit's first Q K^T waits for loads that only began when
+          // this unit's Q was released, and must not hold up this unit's end.
+          const bool last = j + 1 == cur.n_kv;
+          if (!last) {
+            ok = wait_or_abort(&B->kv_full[sn], phn, B, p);
+            for (int hh = 0; ok && hh < NH; ++hh) {
+              ok = wait_or_abort(&B->s_free[hh], gt & 1, B, p);
+              if (!ok) break;
+              tc_fence_after();
+              issue_qk(sn, hh);
+            }
+            if (ok && j + 2 == cur.n_kv) mma_commit(&B->q_empty);
+          }
+          ok = ok && wait_or_abort(&B->v_ready[st], ph, B, p);
+          const uint32_t v_addr = smem_addr(smem + C::kVOff + st * kTileBytes);
           for (int hh = 0; ok && hh < NH; ++hh) {
-            ok = wait_or_abort(&B->s_free[hh], j & 1, B, p);
+            ok = wait_or_abort(&B->p_full[hh], gt & 1, B, p);
             if (!ok) break;
             tc_fence_after();
-            issue_qk(j + 1, hh);
-          }
-        }
-        for (int hh = 0; ok && hh < NH; ++hh) {
-          ok = wait_or_abort(&B->p_full[hh], j & 1, B, p) &&
-               wait_or_abort(&B->v_ready[st], (j / kStages) & 1, B, p);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t v_addr = smem_addr(smem + C::kVOff + st * kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            mma_f16_ts(tmem + C::o_col(hh), tmem + C::p_col(hh) + kk * 8,
-                       desc_sw128(v_addr + kk * 2048, 16, 1024), kIdescPV, (j > 0 || kk > 0));
-          mma_commit(&B->pv_done[hh]);
-          if (hh == NH - 1) mma_commit(&B->kv_empty[st]);
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              mma_f16_ts(tmem + C::o_col(hh), tmem + C::p_col(hh) + kk * 8,
+                         desc_sw128(v_addr + kk * 2048, 16, 1024), kIdescPV, (j > 0 || kk > 0));
+            mma_commit(&B->pv_done[hh]);
+          }
+          if (ok) mma_commit(&B->kv_empty[st]);
+          if (ok && last && has_nxt) {
+            ok = wait_or_abort(&B->kv_full[sn], phn, B, p) &&
+                 wait_or_abort(&B->q_full, (nq + 1) & 1, B, p);
+            for (int hh = 0; ok && hh < NH; ++hh) {
+              ok = wait_or_abort(&B->s_free[hh], gt & 1, B, p);
+              if (!ok) break;
+              tc_fence_after();
+              issue_qk(sn, hh);
+            }
+            if (ok && nxt.n_kv == 1) mma_commit(&B->q_empty);
+          }
+          st = sn;
+          ph = phn;
+          if (++sn == kStages) { sn = 0; phn ^= 1; }
         }
+        if (!ok || !has_nxt) break;
+        cur = nxt;
+        k = kn;
+        ++nq;
       }
       // every MMA issued must be complete before TMEM is released
       mma_commit(&B->mma_done);
@@ -356,31 +498,37 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
     }
   } else {
     // ----------------------------------------------- V conversion (2 warps)
-    // V tile j bf16 -> fp16 in place, 16 bytes at a time (the swizzle only
+    // V tile bf16 -> fp16 in place, 16 bytes at a time (the swizzle only
     // permutes 16-byte chunks within a 128-byte row, so a chunk's row is its
     // offset / 128); keys past the context become 0.
     const int t = (warp - C::kConvWarp) * 32 + lane;
-    for (int j = 0; j < n_kv; ++j) {
-      const int st = j % kStages;
-      const bool ok = wait_or_abort(&B->kv_full[st], (j / kStages) & 1, B, p);
-      if (__any_sync(kFull, !ok)) break;
-      uint8_t* vt = smem + C::kVOff + st * kTileBytes;
+    int gt = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      Unit x;
+      if (!next_unit(k, x)) break;
+      for (int j = 0; j < x.n_kv; ++j, ++gt) {
+        const int st = gt % kStages;
+        ok = wait_or_abort(&B->kv_full[st], (gt / kStages) & 1, B, p);
+        if (__any_sync(kFull, !ok)) { ok = false; break; }
+        uint8_t* vt = smem + C::kVOff + st * kTileBytes;
 #pragma unroll 4
-      for (int c = t; c < static_cast<int>(kTileBytes / 16); c += 64) {
-        uint4 w = *reinterpret_cast<const uint4*>(vt + c * 16);
-        if (j * kBN + (c >> 3) < ctx) {
-          w.x = bf16x2_to_half2(w.x);
-          w.y = bf16x2_to_half2(w.y);
-          w.z = bf16x2_to_half2(w.z);
-          w.w = bf16x2_to_half2(w.w);
-        } else {
-          w = make_uint4(0, 0, 0, 0);
+        for (int e = t; e < static_cast<int>(kTileBytes / 16); e += 64) {
+          uint4 w = *reinterpret_cast<const uint4*>(vt + e * 16);
+          if (j * kBN + (e >> 3) < x.ctx) {
+            w.x = bf16x2_to_half2(w.x);
+            w.y = bf16x2_to_half2(w.y);
+            w.z = bf16x2_to_half2(w.z);
+            w.w = bf16x2_to_half2(w.w);
+          } else {
+            w = make_uint4(0, 0, 0, 0);
+          }
+          *reinterpret_cast<uint4*>(vt + e * 16) = w;
         }
-        *reinterpret_cast<uint4*>(vt + c * 16) = w;
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B->v_ready[st]);
       }
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&B->v_ready[st]);
     }
   }
   } else {
@@ -393,163 +541,195 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
     const uint32_t s_addr = tmem + lane_off + C::s_col(hh);
     const uint32_t o_addr = tmem + lane_off + C::o_col(hh);
     const uint32_t p_addr = tmem + lane_off + C::p_col(hh);
-    const int qpos = pos_first + r;
     const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
-    float m_used = -INFINITY;                           // reference maximum (log2 units)
-    float2 l2 = make_float2(0.f, 0.f);
+    int gt = 0;                                         // global key-tile index
     bool ok = true;
+    bool pending = false;                               // a row copy may still read `stage`
 
-    for (int j = 0; j < n_kv && ok; ++j) {
-      const int key0 = j * kBN;
-      ok = wait_or_abort(&B->s_full[hh], j & 1, B, p);
-      if (__any_sync(kFull, !ok)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t sr[4][32];                               // this row's 128 scores
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
-      tmem_ld_wait();
-      // S_h is in registers: the next tile's Q K^T may overwrite it
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&B->s_free[hh]);
+    for (int k = 0; ok; ++k) {
+      Unit x;
+      if (!next_unit(k, x)) break;
+      const int qpos = x.pos_first + r;
+      const int pos_first = x.pos_first;
+      const int ctx = x.ctx;
+      const int n_kv = x.n_kv;
+      float m_used = -INFINITY;                         // reference maximum (log2 units)
+      float2 l2 = make_float2(0.f, 0.f);
 
-      // Tiles on the causal diagonal or past the context need the mask.
-      const bool masked = (key0 + kBN - 1 > pos_first) || (key0 + kBN > ctx);
-      const int limit = min(qpos, ctx - 1) - key0;     // last visible column
-      // row maximum of the scaled scores of this tile
-      auto tile_max = [&]() -> float {
-        float mt;
-        if (masked) {
-          mt = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              float v = __uint_as_float(sr[c][e]) * p.scale_log2;
-              if (c * 32 + e > limit) v = -INFINITY;
-              mt = fmaxf(mt, v);
-            }
-        } else if (p.scale_log2 >= 0.f) {
-          float mx = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int e = 0; e < 32; e += 2)
-              mx = max3(mx, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-          mt = mx * p.scale_log2;
-        } else {
-          float mn = INFINITY;
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int e = 0; e < 32; e += 2)
-              mn = min3(mn, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-          mt = mn * p.scale_log2;
-        }
-        return mt;
-      };
-      uint32_t pk[2][32];
-      // P = 2^(s * scale * log2e - m) as fp16 pairs; returns the fp32 row sum
-      auto make_p = [&](float mref) -> float2 {
-        const float2 nm2 = make_float2(-mref, -mref);
-        float2 tsum = make_float2(0.f, 0.f);
-        if (masked) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              float2 x = make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-              x = __ffma2_rn(x, sl2, nm2);
-              if (c * 32 + e > limit) x.x = -INFINITY;
-              if (c * 32 + e + 1 > limit) x.y = -INFINITY;
-              const float2 pv = make_float2(ex2(x.x), ex2(x.y));
-              tsum = __fadd2_rn(tsum, pv);
-              pk[c >> 1][(c & 1) * 16 + e / 2] = pack_half2(pv.x, pv.y);
-            }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              float2 x = make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-              x = __ffma2_rn(x, sl2, nm2);
-              const float2 pv = make_float2(ex2(x.x), ex2(x.y));
-              tsum = __fadd2_rn(tsum, pv);
-              pk[c >> 1][(c & 1) * 16 + e / 2] = pack_half2(pv.x, pv.y);
-            }
-        }
-        return tsum;
-      };
-      float f = 1.f;
-      bool move = false;
-      float2 tsum;
-      if (j == 0) {
-        m_used = tile_max();
-        tsum = make_p(m_used == -INFINITY ? 0.f : m_used);
-      } else {
-        // P straight from the reference maximum; only a row sum that shows
-        // some P near the fp16 limit (65504) calls for the tile's maximum
-        tsum = make_p(m_used == -INFINITY ? 0.f : m_used);
-        const float ts = tsum.x + tsum.y;
-        move = !(ts <= 60000.f);
-        if (__any_sync(kFull, move)) {
-          if (move) {
-            const float m_new = fmaxf(m_used, tile_max());
-            f = ex2(m_used - m_new);
-            m_used = m_new;
-          }
-          tsum = make_p(m_used == -INFINITY ? 0.f : m_used);
-        }
-      }
-      // P_h(j-1) must have been consumed (and O_h(j-1) complete) before P_h
-      // is overwritten and O_h rescaled
-      if (j > 0) {
-        ok = wait_or_abort(&B->pv_done[hh], (j - 1) & 1, B, p);
+      for (int j = 0; j < n_kv; ++j, ++gt) {
+        const int key0 = j * kBN;
+        ok = wait_or_abort(&B->s_full[hh], gt & 1, B, p);
         if (__any_sync(kFull, !ok)) { ok = false; break; }
         tc_fence_after();
-        if (__any_sync(kFull, move)) {
+        uint32_t sr[4][32];                             // this row's 128 scores
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t o[32];
-            tmem_ld32(o_addr + c * 32, o);
-            tmem_ld_wait();
+        for (int cc = 0; cc < 4; ++cc) tmem_ld32(s_addr + cc * 32, sr[cc]);
+        tmem_ld_wait();
+        // S_h is in registers: the next tile's Q K^T may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B->s_free[hh]);
+
+        // Tiles on the causal diagonal or past the context need the mask.
+        const bool masked = (key0 + kBN - 1 > pos_first) || (key0 + kBN > ctx);
+        const int limit = min(qpos, ctx - 1) - key0;    // last visible column
+        // row maximum of the scaled scores of this tile
+        auto tile_max = [&]() -> float {
+          float mt;
+          if (masked) {
+            mt = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-            tmem_st32(o_addr + c * 32, o);
+            for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                float v = __uint_as_float(sr[cc][e]) * p.scale_log2;
+                if (cc * 32 + e > limit) v = -INFINITY;
+                mt = fmaxf(mt, v);
+              }
+          } else if (p.scale_log2 >= 0.f) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+              for (int e = 0; e < 32; e += 2)
+                mx = max3(mx, __uint_as_float(sr[cc][e]), __uint_as_float(sr[cc][e + 1]));
+            mt = mx * p.scale_log2;
+          } else {
+            float mn = INFINITY;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+              for (int e = 0; e < 32; e += 2)
+                mn = min3(mn, __uint_as_float(sr[cc][e]), __uint_as_float(sr[cc][e + 1]));
+            mt = mn * p.scale_log2;
+          }
+          return mt;
+        };
+        uint32_t pk[2][32];
+        // P = 2^(s * scale * log2e - m) as fp16 pairs; returns the fp32 row sum
+        auto make_p = [&](float mref) -> float2 {
+          const float2 nm2 = make_float2(-mref, -mref);
+          float2 tsum = make_float2(0.f, 0.f);
+          if (masked) {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+              for (int e = 0; e < 32; e += 2) {
+                float2 v = make_float2(__uint_as_float(sr[cc][e]), __uint_as_float(sr[cc][e + 1]));
+                v = __ffma2_rn(v, sl2, nm2);
+                if (cc * 32 + e > limit) v.x = -INFINITY;
+                if (cc * 32 + e + 1 > limit) v.y = -INFINITY;
+                const float2 pv = make_float2(ex2(v.x), ex2(v.y));
+                tsum = __fadd2_rn(tsum, pv);
+                pk[cc >> 1][(cc & 1) * 16 + e / 2] = pack_half2(pv.x, pv.y);
+              }
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+              for (int e = 0; e < 32; e += 2) {
+                float2 v = make_float2(__uint_as_float(sr[cc][e]), __uint_as_float(sr[cc][e + 1]));
+                v = __ffma2_rn(v, sl2, nm2);
+                const float2 pv = make_float2(ex2(v.x), ex2(v.y));
+                tsum = __fadd2_rn(tsum, pv);
+                pk[cc >> 1][(cc & 1) * 16 + e / 2] = pack_half2(pv.x, pv.y);
+              }
+          }
+          return tsum;
+        };
+        float f = 1.f;
+        bool move = false;
+        float2 tsum;
+        if (j == 0) {
+          m_used = tile_max();
+          tsum = make_p(m_used == -INFINITY ? 0.f : m_used);
+        } else {
+          // P straight from the reference maximum; only a row sum that shows
+          // some P near the fp16 limit (65504) calls for the tile's maximum
+          tsum = make_p(m_used == -INFINITY ? 0.f : m_used);
+          const float ts = tsum.x + tsum.y;
+          move = !(ts <= 60000.f);
+          if (__any_sync(kFull, move)) {
+            if (move) {
+              const float m_new = fmaxf(m_used, tile_max());
+              f = ex2(m_used - m_new);
+              m_used = m_new;
+            }
+            tsum = make_p(m_used == -INFINITY ? 0.f : m_used);
           }
         }
+        // P_h of the previous tile must have been consumed (and O_h
+        // complete) before P_h is overwritten and O_h rescaled.  On a unit's
+        // first tile this was awaited at the end of the previous unit.
+        if (j > 0) {
+          ok = wait_or_abort(&B->pv_done[hh], (gt - 1) & 1, B, p);
+          if (__any_sync(kFull, !ok)) { ok = false; break; }
+          tc_fence_after();
+          if (__any_sync(kFull, move)) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              uint32_t o[32];
+              tmem_ld32(o_addr + cc * 32, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+              tmem_st32(o_addr + cc * 32, o);
+            }
+          }
+        }
+        l2.x = fmaf(l2.x, f, tsum.x);
+        l2.y = fmaf(l2.y, f, tsum.y);
+        tmem_st32(p_addr, pk[0]);
+        tmem_st32(p_addr + 32, pk[1]);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B->p_full[hh]);
       }
-      l2.x = fmaf(l2.x, f, tsum.x);
-      l2.y = fmaf(l2.y, f, tsum.y);
-      tmem_st32(p_addr, pk[0]);
-      tmem_st32(p_addr + 32, pk[1]);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&B->p_full[hh]);
-    }
-    if (ok) {
-      const int jl = n_kv - 1;
-      ok = wait_or_abort(&B->pv_done[hh], jl & 1, B, p);
-    }
-    if (!__any_sync(kFull, !ok)) {
+      if (!ok) break;
+      // the unit's O_h is complete once its last P.V is; read it out before
+      // the next unit's first P.V overwrites it (that P.V waits for this
+      // warpgroup's next p_full)
+      ok = wait_or_abort(&B->pv_done[hh], (gt - 1) & 1, B, p);
+      if (__any_sync(kFull, !ok)) { ok = false; break; }
       tc_fence_after();
       uint32_t o[2][32];
       tmem_ld32(o_addr, o[0]);
       tmem_ld32(o_addr + 32, o[1]);
       tmem_ld_wait();
-      if (r < rows) {
+      // the unit's rows and place, read again rather than held through the loop
+      unit_info<NH, K>(p, tab, static_cast<int>(unit_index(k, c, G)), x);
+      if (r < x.rows) {
+        float4* stage = reinterpret_cast<float4*>(smem + C::kStageOff + (hh * kBM + r) * kOPitch);
+        // the row goes out through its own staging row in shared memory with
+        // one 256-byte bulk copy (direct stores would scatter each warp
+        // instruction over 32 rows 8 KB apart)
+        if (pending) bulk_wait_read();                  // the previous copy has read it
         const float inv = 1.0f / (l2.x + l2.y);
-        float4* dst = reinterpret_cast<float4*>(
-            p.out + (static_cast<long long>(q0 + row0 + r) * p.hq + h0 + hh) * kD);
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
-            dst[c * 8 + e / 4] =
-                make_float4(__uint_as_float(o[c][e]) * inv, __uint_as_float(o[c][e + 1]) * inv,
-                            __uint_as_float(o[c][e + 2]) * inv,
-                            __uint_as_float(o[c][e + 3]) * inv);
+            stage[cc * 8 + e / 4] =
+                make_float4(__uint_as_float(o[cc][e]) * inv, __uint_as_float(o[cc][e + 1]) * inv,
+                            __uint_as_float(o[cc][e + 2]) * inv,
+                            __uint_as_float(o[cc][e + 3]) * inv);
+        fence_async_smem();
+        bulk_store(p.out + (static_cast<long long>(x.q0 + x.row0 + r) * p.hq + x.h0 + hh) * kD,
+                   stage, kD * 4);
+        bulk_commit();
+        pending = true;
+      }
+    }
+    if (pending) bulk_wait_read();
+    if (threadIdx.x == 0) {
+      // units with rows but inconsistent lengths were skipped: say so
+      for (int k = 0;; ++k) {
+        const long long u = unit_index(k, c, G);
+        if (u >= n_units) break;
+        Unit x;
+        unit_info<NH, K>(p, tab, static_cast<int>(u), x);
+        if (x.bad) report(p.status, x.bad_ctx ? TVL_DEV_BAD_CONTEXT_LEN : TVL_DEV_BAD_QUERY_LEN);
       }
     }
   }
@@ -590,7 +770,7 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 
 template <int NH>
 cudaError_t launch_nh(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                      const Params& p, int num_seqs, cudaStream_t stream) {
+                      const Params& p, int num_seqs, int num_sms, cudaStream_t stream) {
   using C = Cfg<NH>;
   // once per device: the shared-memory limit, and the check that the
   // register split fits the registers the block is launched with
@@ -610,9 +790,16 @@ cudaError_t launch_nh(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
     return cudaSuccess;
   });
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>(num_seqs) * p.n_qtiles * (p.hq / NH));
-  return launch_pdl(prefill_kernel<NH>, grid, dim3(C::kThreads), C::kSmemBytes, stream, tq, tk,
-                    tv, p);
+  // persistent: one CTA per SM (at most one per unit), each walking its units
+  const long long units = static_cast<long long>(num_seqs) * p.n_qtiles * (p.hq / NH);
+  dim3 grid(static_cast<unsigned>(units < num_sms ? units : num_sms));
+  // A plain launch, not a programmatic-dependent one: the units are dealt to
+  // the CTAs up front, so the CTAs should start together.  Launched early
+  // behind a kernel that is still draining, they started over that kernel's
+  // tail and the last to start set the end (chunked prefill after the paged
+  // write: 176 us per step against 157 us).
+  prefill_kernel<NH><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -655,8 +842,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.n_qtiles = (a.max_q_len + kBM - 1) / kBM;
   p.scale_log2 = a.scale * kLog2e;
   p.status = a.status;
-  if (p.group >= 2) return launch_nh<2>(tq, tk, tv, p, a.num_seqs, stream);
-  return launch_nh<1>(tq, tk, tv, p, a.num_seqs, stream);
+  if (p.group >= 2) return launch_nh<2>(tq, tk, tv, p, a.num_seqs, a.num_sms, stream);
+  return launch_nh<1>(tq, tk, tv, p, a.num_seqs, a.num_sms, stream);
 }
 
 }  // namespace tvl
