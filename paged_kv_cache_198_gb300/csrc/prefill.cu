@@ -75,9 +75,11 @@ template <int NH>
 struct Cfg {
   static constexpr int kSoftmaxWarps = 4 * NH;
   static constexpr int kProducerWarp = kSoftmaxWarps;
-  static constexpr int kMmaWarp = kSoftmaxWarps + 1;
-  static constexpr int kConvWarp = kSoftmaxWarps + 2;        // two V-conversion warps
+  static constexpr int kMmaWarp = kSoftmaxWarps + 1;         // issues Q K^T
+  static constexpr int kConvWarp = kSoftmaxWarps + 2;        // V conversion
+  static constexpr int kPvWarp = kSoftmaxWarps + 3;          // issues P.V
   static constexpr int kThreads = (kSoftmaxWarps + 4) * 32;
+  static_assert(kConvWarp + 1 == kPvWarp && kThreads == (kPvWarp + 1) * 32, "warp roles");
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKOff = NH * kTileBytes;
   static constexpr uint32_t kVOff = kKOff + kStages * kTileBytes;
@@ -310,7 +312,7 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&B->kv_full[i], 1);
       mbar_init(&B->kv_empty[i], 1);
-      mbar_init(&B->v_ready[i], 2);
+      mbar_init(&B->v_ready[i], 1);
     }
     for (int i = 0; i < NH; ++i) {
       mbar_init(&B->s_full[i], 1);
@@ -318,7 +320,7 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
       mbar_init(&B->p_full[i], 4);
       mbar_init(&B->pv_done[i], 1);
     }
-    mbar_init(&B->mma_done, 1);
+    mbar_init(&B->mma_done, 2);           // one commit from each MMA issuer
     B->abort = 0;
     fence_barrier_init();
   }
@@ -397,99 +399,64 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
         if (!mbar_wait(&B->kv_full[t % kStages], (t / kStages) & 1)) report(p.status, kDevTimeout);
       if (nq > 0 && !mbar_wait(&B->q_full, (nq - 1) & 1)) report(p.status, kDevTimeout);
     }
-  } else if (warp == C::kMmaWarp) {
-    // ---------------------------------------------------------- MMA issuer
-    // One stream of key tiles over all of the CTA's units.  For tile t and
-    // head h, S_h(t+1) = Q_h K(t+1)^T is issued as soon as the softmax has
-    // taken S_h(t) into registers (s_free) -- across a unit boundary too, so
-    // the next unit's first scores are computed during this unit's last
-    // softmax -- then O_h += P_h(t) V(t) once P_h(t) is in TMEM (p_full) and
-    // V(t) is fp16 (v_ready).  After a unit's last Q K^T, q_empty frees the
-    // Q buffer for the next unit.
-    // Lane 0 alone walks the units and issues: the tensor pipe queues
-    // little, so every cycle this thread spends outside tcgen05.mma (waits,
-    // bookkeeping) idles the pipe.
+  } else if (warp == C::kMmaWarp || warp == C::kPvWarp) {
+    // ------------------------------------------------------- MMA issuers
+    // Two threads issue: one the Q K^T MMAs, one the P.V MMAs.  The tensor
+    // pipe queues little, so an issuing thread that waits on a barrier
+    // idles it; with two, one issues while the other waits.  Both walk one
+    // stream of key tiles over all of the CTA's units.
+    //   Q K^T: S_h(t) = Q_h K(t)^T once K(t) has landed and the softmax has
+    //   taken S_h(t-1) into registers (s_free) -- across unit boundaries too,
+    //   so the next unit's first scores are ready when its softmax starts.
+    //   After a unit's last Q K^T, q_empty frees the Q buffer.
+    //   P.V: O_h += P_h(t) V(t) once P_h(t) is in TMEM (p_full) and V(t) is
+    //   fp16 (v_ready); then the stage goes back to the producer (kv_empty:
+    //   Q K^T(t) is complete too, the softmax having read S_h(t)).
     if (lane == 0) {
-      auto next_unit1 = [&](int& k, Unit& x) -> bool {
-        return next_valid_unit<NH, K, false>(p, tab_or_null, k, x);
-      };
+      const bool is_qk = warp == C::kMmaWarp;
       const uint32_t q_addr = smem_addr(smem + C::kQOff);
-      auto issue_qk = [&](int st, int hh) {
-        const uint32_t k_addr = smem_addr(smem + C::kKOff + st * kTileBytes);
-        const uint32_t qa = q_addr + hh * kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_f16_ss(tmem + C::s_col(hh), desc_sw128(qa + kk * 32, 16, 1024),
-                     desc_sw128(k_addr + kk * 32, 16, 1024), kIdescQK, kk > 0);
-        mma_commit(&B->s_full[hh]);
-      };
-      int k = 0;
-      Unit cur;
-      bool ok = next_unit1(k, cur);
-      int gt = 0;                                       // tile whose P.V comes next
-      int nq = 0;                                       // index of cur among the units
-      if (ok) {
-        ok = wait_or_abort(&B->q_full, 0, B, p) && wait_or_abort(&B->kv_full[0], 0, B, p);
-        if (ok) {
-          tc_fence_after();
-          for (int hh = 0; hh < NH; ++hh) issue_qk(0, hh);
-          if (cur.n_kv == 1) mma_commit(&B->q_empty);
-        }
-      }
-      // stage and phase of tile gt (P.V next) and of tile gt + 1 (Q K^T next)
-      int st = 0, ph = 0;
-      int sn = kStages > 1 ? 1 : 0, phn = kStages > 1 ? 0 : 1;
-      while (ok) {
-        int kn = k + 1;
-        Unit nxt;
-        const bool has_nxt = next_unit1(kn, nxt);
-        for (int j = 0; ok && j < cur.n_kv; ++j, ++gt) {
-          // Within a unit the next S comes first, so the tensor pipe works
-          // while P is computed.  On a unit's last tile its P.V comes first:
-          // the next unit's first Q K^T waits for loads that only began when
-          // this unit's Q was released, and must not hold up this unit's end.
-          const bool last = j + 1 == cur.n_kv;
-          if (!last) {
-            ok = wait_or_abort(&B->kv_full[sn], phn, B, p);
+      int gt = 0;                                       // key tile of the stream
+      int st = 0, ph = 0;                               // its stage and phase
+      int nq = 0;                                       // units begun
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        Unit x;
+        if (!next_valid_unit<NH, K, false>(p, tab_or_null, k, x)) break;
+        for (int j = 0; ok && j < x.n_kv; ++j, ++gt) {
+          if (is_qk) {
+            ok = wait_or_abort(&B->kv_full[st], ph, B, p);
+            if (ok && j == 0) ok = wait_or_abort(&B->q_full, nq & 1, B, p);
+            const uint32_t k_addr = smem_addr(smem + C::kKOff + st * kTileBytes);
             for (int hh = 0; ok && hh < NH; ++hh) {
-              ok = wait_or_abort(&B->s_free[hh], gt & 1, B, p);
+              if (gt > 0) ok = wait_or_abort(&B->s_free[hh], (gt - 1) & 1, B, p);
               if (!ok) break;
               tc_fence_after();
-              issue_qk(sn, hh);
-            }
-            if (ok && j + 2 == cur.n_kv) mma_commit(&B->q_empty);
-          }
-          ok = ok && wait_or_abort(&B->v_ready[st], ph, B, p);
-          const uint32_t v_addr = smem_addr(smem + C::kVOff + st * kTileBytes);
-          for (int hh = 0; ok && hh < NH; ++hh) {
-            ok = wait_or_abort(&B->p_full[hh], gt & 1, B, p);
-            if (!ok) break;
-            tc_fence_after();
+              const uint32_t qa = q_addr + hh * kTileBytes;
 #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)
-              mma_f16_ts(tmem + C::o_col(hh), tmem + C::p_col(hh) + kk * 8,
-                         desc_sw128(v_addr + kk * 2048, 16, 1024), kIdescPV, (j > 0 || kk > 0));
-            mma_commit(&B->pv_done[hh]);
-          }
-          if (ok) mma_commit(&B->kv_empty[st]);
-          if (ok && last && has_nxt) {
-            ok = wait_or_abort(&B->kv_full[sn], phn, B, p) &&
-                 wait_or_abort(&B->q_full, (nq + 1) & 1, B, p);
+              for (int kk = 0; kk < kD / 16; ++kk)
+                mma_f16_ss(tmem + C::s_col(hh), desc_sw128(qa + kk * 32, 16, 1024),
+                           desc_sw128(k_addr + kk * 32, 16, 1024), kIdescQK, kk > 0);
+              mma_commit(&B->s_full[hh]);
+            }
+            if (ok && j + 1 == x.n_kv) mma_commit(&B->q_empty);
+          } else {
+            ok = wait_or_abort(&B->v_ready[st], ph, B, p);
+            const uint32_t v_addr = smem_addr(smem + C::kVOff + st * kTileBytes);
             for (int hh = 0; ok && hh < NH; ++hh) {
-              ok = wait_or_abort(&B->s_free[hh], gt & 1, B, p);
+              ok = wait_or_abort(&B->p_full[hh], gt & 1, B, p);
               if (!ok) break;
               tc_fence_after();
-              issue_qk(sn, hh);
+#pragma unroll
+              for (int kk = 0; kk < kBN / 16; ++kk)
+                mma_f16_ts(tmem + C::o_col(hh), tmem + C::p_col(hh) + kk * 8,
+                           desc_sw128(v_addr + kk * 2048, 16, 1024), kIdescPV,
+                           (j > 0 || kk > 0));
+              mma_commit(&B->pv_done[hh]);
             }
-            if (ok && nxt.n_kv == 1) mma_commit(&B->q_empty);
+            if (ok) mma_commit(&B->kv_empty[st]);
           }
-          st = sn;
-          ph = phn;
-          if (++sn == kStages) { sn = 0; phn ^= 1; }
+          if (++st == kStages) { st = 0; ph ^= 1; }
         }
-        if (!ok || !has_nxt) break;
-        cur = nxt;
-        k = kn;
         ++nq;
       }
       // every MMA issued must be complete before TMEM is released
@@ -497,11 +464,11 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
       if (!mbar_wait(&B->mma_done, 0)) report(p.status, kDevTimeout);
     }
   } else {
-    // ----------------------------------------------- V conversion (2 warps)
+    // ------------------------------------------------------- V conversion
     // V tile bf16 -> fp16 in place, 16 bytes at a time (the swizzle only
     // permutes 16-byte chunks within a 128-byte row, so a chunk's row is its
     // offset / 128); keys past the context become 0.
-    const int t = (warp - C::kConvWarp) * 32 + lane;
+    const int t = lane;
     int gt = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -513,7 +480,7 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
         if (__any_sync(kFull, !ok)) { ok = false; break; }
         uint8_t* vt = smem + C::kVOff + st * kTileBytes;
 #pragma unroll 4
-        for (int e = t; e < static_cast<int>(kTileBytes / 16); e += 64) {
+        for (int e = t; e < static_cast<int>(kTileBytes / 16); e += 32) {
           uint4 w = *reinterpret_cast<const uint4*>(vt + e * 16);
           if (j * kBN + (e >> 3) < x.ctx) {
             w.x = bf16x2_to_half2(w.x);
