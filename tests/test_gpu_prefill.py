@@ -134,6 +134,33 @@ def test_prefill_scores_rising_along_the_context(rise):
     assert_clean_status()
 
 
+@pytest.mark.parametrize("hkv", [2, 8])     # two query heads per unit / one
+def test_prefill_inconsistent_lengths_are_reported_and_skipped(hkv):
+    """One sequence whose context is shorter than its chunk, one whose context
+    runs past its block table: their rows are left alone and the status word
+    says why, while the other sequence is computed as usual."""
+    wl = W.make_prefill(732, [30, 50, 70], [40, 20, 130], num_q_heads=8, num_kv_heads=hkv,
+                        block_size=16)
+    t = W.to_device(wl, DEV)
+    tvl.paged_kv_write(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["slot_mapping"])
+    ctx = t["context_lens"].clone()
+    ctx[1] = 19                                   # < Lq = 20
+    ctx[2] = wl.max_blocks_per_seq * wl.block_size + 1
+    out = torch.full(tuple(wl.q.shape), float("nan"), dtype=torch.float32, device=DEV)
+    tvl.paged_attention_prefill(out, t["q"], t["query_start_loc"], t["k_cache"], t["v_cache"],
+                                t["block_tables"], ctx, wl.scale, wl.max_q_len)
+    torch.cuda.synchronize()
+    bits = tvl.get_device_status()
+    assert bits & tvl.DEV_BAD_QUERY_LEN
+    assert bits & tvl.DEV_BAD_CONTEXT_LEN
+    got = out.double().cpu().numpy()
+    qsl = wl.query_start_loc.tolist()
+    ref = oracle_prefill(wl)
+    assert_close(got[qsl[0]:qsl[1]], ref[qsl[0]:qsl[1]], "valid sequence")
+    assert np.isnan(got[qsl[1]:qsl[3]]).all()
+    assert_clean_status()
+
+
 def test_prefill_poisoned_unused_slots():
     wl = W.make_prefill(721, [3, 40, 200], [10, 100, 60], num_q_heads=8, num_kv_heads=2,
                         block_size=32)
