@@ -114,7 +114,6 @@ struct Barriers {
   uint64_t pv_done[2];
   uint64_t mma_done;
   uint32_t tmem_base;
-  uint32_t abort;
 };
 static_assert(sizeof(Barriers) <= 512, "barrier area");
 
@@ -156,13 +155,11 @@ __device__ __forceinline__ uint32_t bf16x2_to_half2(uint32_t w) {
   return pack_half2(f.x, f.y);
 }
 
-// Bounded wait that records a timeout in the status word and in the CTA's
-// abort flag; returns false when the caller must stop.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Barriers* B,
-                                              const Params& p) {
+// Bounded wait that records a timeout in the status word; returns false
+// when the caller must stop (every role then leaves its loop).
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const Params& p) {
   if (mbar_wait(bar, parity)) return true;
   report(p.status, kDevTimeout);
-  atomicExch(&B->abort, 1u);
   return false;
 }
 
@@ -301,9 +298,8 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
     }
     tab = t;
   }
-  const int* tab_or_null = n_items <= K ? reinterpret_cast<const int*>(smem + C::kTabOff) : nullptr;
   auto next_unit = [&](int& k, Unit& x) -> bool {
-    return next_valid_unit<NH, K, true>(p, tab_or_null, k, x);
+    return next_valid_unit<NH, K, true>(p, tab, k, x);
   };
 
   if (threadIdx.x == 0) {
@@ -321,7 +317,6 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
       mbar_init(&B->pv_done[i], 1);
     }
     mbar_init(&B->mma_done, 2);           // one commit from each MMA issuer
-    B->abort = 0;
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -353,7 +348,7 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
       Unit x;
       if (!next_unit(k, x)) break;
       if (lane == 0) {
-        if (nq > 0) ok = wait_or_abort(&B->q_empty, (nq - 1) & 1, B, p);
+        if (nq > 0) ok = wait_or_abort(&B->q_empty, (nq - 1) & 1, p);
         if (ok) {
           mbar_arrive_expect_tx(&B->q_full, NH * kTileBytes);
           for (int i = 0; i < NH; ++i)
@@ -370,7 +365,7 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
       for (int j = 0; j < x.n_kv; ++j, ++gt) {
         const int st = gt % kStages;
         if (gt >= kStages && lane == 0)
-          ok = wait_or_abort(&B->kv_empty[st], ((gt / kStages) - 1) & 1, B, p);
+          ok = wait_or_abort(&B->kv_empty[st], ((gt / kStages) - 1) & 1, p);
         ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
         if (lane == 0) mbar_arrive_expect_tx(&B->kv_full[st], 2 * kTileBytes);
@@ -421,14 +416,14 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
       bool ok = true;
       for (int k = 0; ok; ++k) {
         Unit x;
-        if (!next_valid_unit<NH, K, false>(p, tab_or_null, k, x)) break;
+        if (!next_valid_unit<NH, K, false>(p, tab, k, x)) break;
         for (int j = 0; ok && j < x.n_kv; ++j, ++gt) {
           if (is_qk) {
-            ok = wait_or_abort(&B->kv_full[st], ph, B, p);
-            if (ok && j == 0) ok = wait_or_abort(&B->q_full, nq & 1, B, p);
+            ok = wait_or_abort(&B->kv_full[st], ph, p);
+            if (ok && j == 0) ok = wait_or_abort(&B->q_full, nq & 1, p);
             const uint32_t k_addr = smem_addr(smem + C::kKOff + st * kTileBytes);
             for (int hh = 0; ok && hh < NH; ++hh) {
-              if (gt > 0) ok = wait_or_abort(&B->s_free[hh], (gt - 1) & 1, B, p);
+              if (gt > 0) ok = wait_or_abort(&B->s_free[hh], (gt - 1) & 1, p);
               if (!ok) break;
               tc_fence_after();
               const uint32_t qa = q_addr + hh * kTileBytes;
@@ -440,10 +435,10 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
             }
             if (ok && j + 1 == x.n_kv) mma_commit(&B->q_empty);
           } else {
-            ok = wait_or_abort(&B->v_ready[st], ph, B, p);
+            ok = wait_or_abort(&B->v_ready[st], ph, p);
             const uint32_t v_addr = smem_addr(smem + C::kVOff + st * kTileBytes);
             for (int hh = 0; ok && hh < NH; ++hh) {
-              ok = wait_or_abort(&B->p_full[hh], gt & 1, B, p);
+              ok = wait_or_abort(&B->p_full[hh], gt & 1, p);
               if (!ok) break;
               tc_fence_after();
 #pragma unroll
@@ -476,7 +471,7 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
       if (!next_unit(k, x)) break;
       for (int j = 0; j < x.n_kv; ++j, ++gt) {
         const int st = gt % kStages;
-        ok = wait_or_abort(&B->kv_full[st], (gt / kStages) & 1, B, p);
+        ok = wait_or_abort(&B->kv_full[st], (gt / kStages) & 1, p);
         if (__any_sync(kFull, !ok)) { ok = false; break; }
         uint8_t* vt = smem + C::kVOff + st * kTileBytes;
 #pragma unroll 4
@@ -525,7 +520,7 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
 
       for (int j = 0; j < n_kv; ++j, ++gt) {
         const int key0 = j * kBN;
-        ok = wait_or_abort(&B->s_full[hh], gt & 1, B, p);
+        ok = wait_or_abort(&B->s_full[hh], gt & 1, p);
         if (__any_sync(kFull, !ok)) { ok = false; break; }
         tc_fence_after();
         uint32_t sr[4][32];                             // this row's 128 scores
@@ -629,7 +624,7 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
         // complete) before P_h is overwritten and O_h rescaled.  On a unit's
         // first tile this was awaited at the end of the previous unit.
         if (j > 0) {
-          ok = wait_or_abort(&B->pv_done[hh], (gt - 1) & 1, B, p);
+          ok = wait_or_abort(&B->pv_done[hh], (gt - 1) & 1, p);
           if (__any_sync(kFull, !ok)) { ok = false; break; }
           tc_fence_after();
           if (__any_sync(kFull, move)) {
@@ -657,7 +652,7 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
       // the unit's O_h is complete once its last P.V is; read it out before
       // the next unit's first P.V overwrites it (that P.V waits for this
       // warpgroup's next p_full)
-      ok = wait_or_abort(&B->pv_done[hh], (gt - 1) & 1, B, p);
+      ok = wait_or_abort(&B->pv_done[hh], (gt - 1) & 1, p);
       if (__any_sync(kFull, !ok)) { ok = false; break; }
       tc_fence_after();
       uint32_t o[2][32];
