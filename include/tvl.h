@@ -213,9 +213,14 @@ tvl_status tvl_paged_decode_step(
  *   out  : float32 [Tq, Hq, D]; q : bf16 [Tq, Hq, D]        (device)
  *   query_start_loc : int32 [S + 1], non-decreasing, [0] = 0, [S] = Tq
  *   block_tables : int32 [S, MB]; context_lens : int32 [S]  (device)
- * max_q_len must be >= every Lq (it sizes the grid).  Lq > context_lens[s]
- * is invalid on the device (rows are left unwritten, TVL_DEV_BAD_QUERY_LEN).
- * Supported: D == 64, G in {1, 2, 4, 8}, bs in {16, 32, 64, 128}, Hkv <= 255.
+ * max_q_len must be >= every Lq (it sets the number of 128-row query tiles
+ * per sequence).  On the device, Lq > context_lens[s] (TVL_DEV_BAD_QUERY_LEN)
+ * and context_lens[s] > MB * bs (TVL_DEV_BAD_CONTEXT_LEN) are reported and
+ * that sequence's rows are left unwritten.
+ * Supported: D == 64, G in {1, 2, 4, 8}, bs in {16, 32, 64, 128}, Hkv <= 255,
+ * num_seqs <= 65535 and num_seqs * ceil(max_q_len / 128) * Hq < 2^31
+ * (else TVL_ERR_UNSUPPORTED).  The call launches one kernel (at most one
+ * block per SM) and allocates nothing.
  */
 tvl_status tvl_paged_attention_prefill(
     float* out, const void* q, const int32_t* query_start_loc,
