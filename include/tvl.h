@@ -77,9 +77,15 @@ typedef enum {
 #define TVL_DEV_BAD_SLOT        0x1  /* slot_mapping entry >= NB * bs            */
 #define TVL_DEV_BAD_BLOCK_ID    0x2  /* block table entry outside [0, NB)        */
 #define TVL_DEV_BAD_CONTEXT_LEN 0x4  /* context length < 0 or > MB * bs          */
-#define TVL_DEV_BAD_QUERY_LEN   0x8  /* prefill: query length > context length   */
+#define TVL_DEV_BAD_QUERY_LEN   0x8  /* prefill: query rows outside [0, Tq),
+                                        more than max_q_len, or more than the
+                                        context length                          */
 #define TVL_DEV_TIMEOUT         0x10 /* a kernel's bounded wait gave up (~1 s);
                                         its CTA left after its copies landed    */
+#define TVL_DEV_NONFINITE       0x20 /* prefill: an output row is not finite --
+                                        a V value with |v| > 65504 (beyond the
+                                        fp16 range its P.V uses) or non-finite
+                                        inputs                                  */
 
 /*
  * Paged KV write [tiny-vllm README, curriculum "Paged KV cache" and "Why KV
@@ -214,9 +220,18 @@ tvl_status tvl_paged_decode_step(
  *   query_start_loc : int32 [S + 1], non-decreasing, [0] = 0, [S] = Tq
  *   block_tables : int32 [S, MB]; context_lens : int32 [S]  (device)
  * max_q_len must be >= every Lq (it sets the number of 128-row query tiles
- * per sequence).  On the device, Lq > context_lens[s] (TVL_DEV_BAD_QUERY_LEN)
- * and context_lens[s] > MB * bs (TVL_DEV_BAD_CONTEXT_LEN) are reported and
- * that sequence's rows are left unwritten.
+ * per sequence).  On the device, a sequence whose rows would leave [0, Tq)
+ * (query_start_loc[s] < 0, a decreasing entry, or query_start_loc[s+1] > Tq),
+ * whose Lq exceeds max_q_len rounded up to 128, or whose Lq exceeds
+ * context_lens[s] is reported (TVL_DEV_BAD_QUERY_LEN), as is a context
+ * longer than MB * bs (TVL_DEV_BAD_CONTEXT_LEN); such a sequence's rows are
+ * left unwritten and nothing outside `out` is touched.
+ * Precision: P and V enter the P.V product as fp16 (P rounded to 2^-11
+ * relative, exact where the sum is taken in fp32).  V values must lie within
+ * the fp16 range, |v| <= 65504 (bf16 can hold more): a larger one makes
+ * the output rows of the query tiles whose key range holds it inf or NaN,
+ * and any output row that is not finite sets TVL_DEV_NONFINITE.  V values
+ * below 2^-14 in magnitude keep an absolute error under 2^-25.
  * Supported: D == 64, G in {1, 2, 4, 8}, bs in {16, 32, 64, 128}, Hkv <= 255,
  * num_seqs <= 65535 and num_seqs * ceil(max_q_len / 128) * Hq < 2^31
  * (else TVL_ERR_UNSUPPORTED).  The call launches one kernel (at most one

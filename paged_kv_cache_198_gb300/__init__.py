@@ -8,7 +8,16 @@ been built, every call raises ``TvlError``.
 
 Functions (same names as the C entry points, without the ``tvl_`` prefix):
   paged_kv_write, paged_attention_decode, paged_attention_decode_workspace_size,
-  paged_attention_prefill, get_device_status, version.
+  paged_decode_step, paged_attention_prefill, rope_paged_kv_write,
+  copy_blocks, get_device_status, version.
+
+Bound calls (``bind_paged_decode_step``, ``bind_paged_attention_decode``,
+``bind_paged_attention_prefill``, ``bind_paged_kv_write``) check their
+tensors once and return a callable that re-issues the same C call -- same
+pointers, sizes and stream -- with one ctypes call and no further checks.
+They are for loops that call the library with the same buffers every step
+(a serving loop, a benchmark): the tensors must keep their storage, and the
+device that was current at bind time must be current when the call is made.
 """
 from __future__ import annotations
 
@@ -23,7 +32,9 @@ __all__ = [
     "rope_paged_kv_write",
     "paged_attention_decode_workspace_size", "paged_attention_prefill", "get_device_status",
     "version", "library_path", "DEV_BAD_SLOT", "DEV_BAD_BLOCK_ID", "DEV_BAD_CONTEXT_LEN",
-    "DEV_BAD_QUERY_LEN", "DEV_TIMEOUT", "selftest_bounded_wait", "paged_decode_step",
+    "DEV_BAD_QUERY_LEN", "DEV_TIMEOUT", "DEV_NONFINITE", "selftest_bounded_wait",
+    "paged_decode_step", "BoundCall", "bind_paged_decode_step", "bind_paged_attention_decode",
+    "bind_paged_attention_prefill", "bind_paged_kv_write",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -33,6 +44,7 @@ _LIB_PATH = os.path.join(_PKG, "libtvl.so")
  ERR_OUT_OF_BLOCKS) = range(7)
 DEV_BAD_SLOT, DEV_BAD_BLOCK_ID, DEV_BAD_CONTEXT_LEN, DEV_BAD_QUERY_LEN, DEV_TIMEOUT = (
     0x1, 0x2, 0x4, 0x8, 0x10)
+DEV_NONFINITE = 0x20
 
 _lock = threading.Lock()
 _lib = None
@@ -170,9 +182,7 @@ def version() -> int:
     return int(_load().tvl_version())
 
 
-def paged_kv_write(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None) -> None:
-    """k_cache/v_cache bf16 [NB, bs, Hkv, D] (in place) <- k_new/v_new bf16
-    [T, Hkv, D] at rows slot_mapping int32 [T] (negative = skip)."""
+def _prep_kv_write(k_new, v_new, k_cache, v_cache, slot_mapping, stream):
     _need(k_cache, "k_cache", torch.bfloat16, 4)
     dev = k_cache.get_device()
     _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
@@ -186,9 +196,22 @@ def paged_kv_write(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None) ->
     if k_new.shape != (t, hkv, d) or v_new.shape != (t, hkv, d):
         raise ValueError(f"k_new/v_new must be [{t}, {hkv}, {d}]")
     with _on_device(dev):
-        _check(_load().tvl_paged_kv_write(_ptr(k_new), _ptr(v_new), _ptr(k_cache),
-                                          _ptr(v_cache), _ptr(slot_mapping), t, hkv, d, bs, nb,
-                                          _stream(stream)))
+        args = (_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping),
+                t, hkv, d, bs, nb, _stream(stream))
+    return dev, _load().tvl_paged_kv_write, args, (k_new, v_new, k_cache, v_cache, slot_mapping)
+
+
+def paged_kv_write(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None) -> None:
+    """k_cache/v_cache bf16 [NB, bs, Hkv, D] (in place) <- k_new/v_new bf16
+    [T, Hkv, D] at rows slot_mapping int32 [T] (negative = skip)."""
+    dev, fn, args, _ = _prep_kv_write(k_new, v_new, k_cache, v_cache, slot_mapping, stream)
+    with _on_device(dev):
+        _check(fn(*args))
+
+
+def bind_paged_kv_write(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None):
+    """paged_kv_write, checked once; returns a BoundCall."""
+    return BoundCall(*_prep_kv_write(k_new, v_new, k_cache, v_cache, slot_mapping, stream))
 
 
 def rope_paged_kv_write(q, k_new, v_new, k_cache, v_cache, slot_mapping, positions,
@@ -240,10 +263,19 @@ def paged_attention_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, h
 _ws_sizes = {}
 
 
-def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
-                           partition_size=0, workspace=None, stream=None):
-    """out fp32 [S, Hq, D] <- paged decode attention of q bf16 [S, Hq, D].
-    workspace: uint8 CUDA tensor (allocated here when None and needed)."""
+def _workspace_for(dev, s, hq, hkv, d, mb, bs, partition_size, workspace):
+    need = paged_attention_decode_workspace_size(s, hq, hkv, d, mb, bs, partition_size)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8, 1, dev)
+    return workspace, (workspace.numel() if workspace is not None else 0)
+
+
+def _prep_decode(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale,
+                 partition_size, workspace, stream):
+    """Checks of a decode (k_new is None) or decode-step call; returns the
+    device, the C function, its arguments and the tensors they point into."""
     _need(k_cache, "k_cache", torch.bfloat16, 4)
     dev = k_cache.get_device()
     _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
@@ -257,19 +289,44 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
         raise ValueError("inconsistent q / out / cache shapes")
     if block_tables.shape[0] != s or context_lens.shape[0] != s:
         raise ValueError("block_tables / context_lens must have num_seqs rows")
+    step = k_new is not None
+    if step:
+        _need(k_new, "k_new", torch.bfloat16, 3, dev)
+        _need(v_new, "v_new", torch.bfloat16, 3, dev)
+        if tuple(k_new.shape) != (s, hkv, d) or v_new.shape != k_new.shape:
+            raise ValueError("k_new / v_new must be [num_seqs, num_kv_heads, head_dim]")
     mb = block_tables.shape[1]
     with _on_device(dev):
-        need = paged_attention_decode_workspace_size(s, hq, hkv, d, mb, bs, partition_size)
-        if workspace is None and need > 0:
-            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
-        if workspace is not None:
-            _need(workspace, "workspace", torch.uint8, 1, dev)
-        ws_bytes = workspace.numel() if workspace is not None else 0
-        _check(_load().tvl_paged_attention_decode(
-            _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-            _ptr(context_lens), s, hq, hkv, d, bs, nb, mb, float(scale), int(partition_size),
-            _ptr(workspace), ws_bytes, _stream(stream)))
+        workspace, ws_bytes = _workspace_for(dev, s, hq, hkv, d, mb, bs, int(partition_size),
+                                             workspace)
+        tail = (_ptr(block_tables), _ptr(context_lens), s, hq, hkv, d, bs, nb, mb,
+                float(scale), int(partition_size), _ptr(workspace), ws_bytes, _stream(stream))
+    lib = _load()
+    keep = (out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, workspace)
+    if step:
+        return dev, lib.tvl_paged_decode_step, (
+            _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache)) + tail, keep
+    return dev, lib.tvl_paged_attention_decode, (
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache)) + tail, keep
+
+
+def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                           partition_size=0, workspace=None, stream=None):
+    """out fp32 [S, Hq, D] <- paged decode attention of q bf16 [S, Hq, D].
+    workspace: uint8 CUDA tensor (allocated here when None and needed)."""
+    dev, fn, args, _ = _prep_decode(out, q, None, None, k_cache, v_cache, block_tables,
+                                    context_lens, scale, partition_size, workspace, stream)
+    with _on_device(dev):
+        _check(fn(*args))
     return out
+
+
+def bind_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                                partition_size=0, workspace=None, stream=None):
+    """paged_attention_decode, checked once (the workspace, when None and
+    needed, is allocated here once); returns a BoundCall."""
+    return BoundCall(*_prep_decode(out, q, None, None, k_cache, v_cache, block_tables,
+                                   context_lens, scale, partition_size, workspace, stream))
 
 
 def paged_decode_step(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale,
@@ -278,42 +335,26 @@ def paged_decode_step(out, q, k_new, v_new, k_cache, v_cache, block_tables, cont
     [S, Hkv, D] at position context_lens[s] - 1 of each sequence, then
     out fp32 [S, Hq, D] <- paged decode attention of q bf16 [S, Hq, D] over
     the updated cache."""
-    _need(k_cache, "k_cache", torch.bfloat16, 4)
-    dev = k_cache.get_device()
-    _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
-    _need(q, "q", torch.bfloat16, 3, dev)
-    _need(k_new, "k_new", torch.bfloat16, 3, dev)
-    _need(v_new, "v_new", torch.bfloat16, 3, dev)
-    _need(out, "out", torch.float32, 3, dev)
-    _need(block_tables, "block_tables", torch.int32, 2, dev)
-    _need(context_lens, "context_lens", torch.int32, 1, dev)
-    nb, bs, hkv, d = k_cache.shape
-    s, hq, d2 = q.shape
-    if d2 != d or out.shape != q.shape or v_cache.shape != k_cache.shape:
-        raise ValueError("inconsistent q / out / cache shapes")
-    if tuple(k_new.shape) != (s, hkv, d) or v_new.shape != k_new.shape:
-        raise ValueError("k_new / v_new must be [num_seqs, num_kv_heads, head_dim]")
-    if block_tables.shape[0] != s or context_lens.shape[0] != s:
-        raise ValueError("block_tables / context_lens must have num_seqs rows")
-    mb = block_tables.shape[1]
+    if k_new is None or v_new is None:
+        raise TypeError("k_new and v_new are required")
+    dev, fn, args, _ = _prep_decode(out, q, k_new, v_new, k_cache, v_cache, block_tables,
+                                    context_lens, scale, partition_size, workspace, stream)
     with _on_device(dev):
-        need = paged_attention_decode_workspace_size(s, hq, hkv, d, mb, bs, partition_size)
-        if workspace is None and need > 0:
-            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
-        if workspace is not None:
-            _need(workspace, "workspace", torch.uint8, 1, dev)
-        ws_bytes = workspace.numel() if workspace is not None else 0
-        _check(_load().tvl_paged_decode_step(
-            _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
-            _ptr(block_tables), _ptr(context_lens), s, hq, hkv, d, bs, nb, mb, float(scale),
-            int(partition_size), _ptr(workspace), ws_bytes, _stream(stream)))
+        _check(fn(*args))
     return out
 
 
-def paged_attention_prefill(out, q, query_start_loc, k_cache, v_cache, block_tables,
-                            context_lens, scale, max_q_len, stream=None):
-    """out fp32 [Tq, Hq, D] <- causal attention of the last Lq tokens of each
-    sequence (q bf16 [Tq, Hq, D], packed by query_start_loc int32 [S+1])."""
+def bind_paged_decode_step(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                           scale, partition_size=0, workspace=None, stream=None):
+    """paged_decode_step, checked once; returns a BoundCall."""
+    if k_new is None or v_new is None:
+        raise TypeError("k_new and v_new are required")
+    return BoundCall(*_prep_decode(out, q, k_new, v_new, k_cache, v_cache, block_tables,
+                                   context_lens, scale, partition_size, workspace, stream))
+
+
+def _prep_prefill(out, q, query_start_loc, k_cache, v_cache, block_tables, context_lens, scale,
+                  max_q_len, stream):
     _need(k_cache, "k_cache", torch.bfloat16, 4)
     dev = k_cache.get_device()
     _need(v_cache, "v_cache", torch.bfloat16, 4, dev)
@@ -331,11 +372,50 @@ def paged_attention_prefill(out, q, query_start_loc, k_cache, v_cache, block_tab
         raise ValueError("query_start_loc must be [S+1] and block_tables [S, MB]")
     mb = block_tables.shape[1]
     with _on_device(dev):
-        _check(_load().tvl_paged_attention_prefill(
-            _ptr(out), _ptr(q), _ptr(query_start_loc), _ptr(k_cache), _ptr(v_cache),
-            _ptr(block_tables), _ptr(context_lens), s, tq, int(max_q_len), hq, hkv, d, bs, nb,
-            mb, float(scale), _stream(stream)))
+        args = (_ptr(out), _ptr(q), _ptr(query_start_loc), _ptr(k_cache), _ptr(v_cache),
+                _ptr(block_tables), _ptr(context_lens), s, tq, int(max_q_len), hq, hkv, d, bs,
+                nb, mb, float(scale), _stream(stream))
+    keep = (out, q, query_start_loc, k_cache, v_cache, block_tables, context_lens)
+    return dev, _load().tvl_paged_attention_prefill, args, keep
+
+
+def paged_attention_prefill(out, q, query_start_loc, k_cache, v_cache, block_tables,
+                            context_lens, scale, max_q_len, stream=None):
+    """out fp32 [Tq, Hq, D] <- causal attention of the last Lq tokens of each
+    sequence (q bf16 [Tq, Hq, D], packed by query_start_loc int32 [S+1])."""
+    dev, fn, args, _ = _prep_prefill(out, q, query_start_loc, k_cache, v_cache, block_tables,
+                                     context_lens, scale, max_q_len, stream)
+    with _on_device(dev):
+        _check(fn(*args))
     return out
+
+
+def bind_paged_attention_prefill(out, q, query_start_loc, k_cache, v_cache, block_tables,
+                                 context_lens, scale, max_q_len, stream=None):
+    """paged_attention_prefill, checked once; returns a BoundCall."""
+    return BoundCall(*_prep_prefill(out, q, query_start_loc, k_cache, v_cache, block_tables,
+                                    context_lens, scale, max_q_len, stream))
+
+
+class BoundCall:
+    """One C-ABI call whose arguments were checked and converted once.
+    Calling it re-issues the call (same pointers, sizes and stream); a non-OK
+    status raises TvlError.  It keeps references to the tensors it points
+    into; they must keep their storage, and the bind-time device must be
+    current when it is called."""
+
+    __slots__ = ("device", "_fn", "_args", "_keep")
+
+    def __init__(self, device, fn, args, keep):
+        self.device = device
+        self._fn = fn
+        self._args = args
+        self._keep = keep
+
+    def __call__(self) -> None:
+        rc = self._fn(*self._args)
+        if rc:
+            _check(rc)
 
 
 def selftest_bounded_wait(stream=None) -> None:

@@ -38,8 +38,12 @@
 //             next tile's S is issued as soon as the softmax has released S,
 //             before this tile's P.V (on a unit's last tile, after it).
 //             Completion is signalled by tcgen05.commit;
-//   4NH+2,+3  V conversion: each V tile bf16 -> fp16 in place (exact for
-//             |v| >= 2^-14; keys past the context become 0).
+//   4NH+2     V conversion: each V tile bf16 -> fp16 in place (exact for
+//             2^-14 <= |v| <= 65504; smaller values keep an absolute error
+//             below 2^-25; a larger one becomes infinite, which leaves rows
+//             that are not finite, reported as TVL_DEV_NONFINITE; keys past
+//             the context become 0);
+//   4NH+3     P.V issuer (below).
 // P and V go through fp16 rather than bf16 so that rounding P costs at most
 // 2^-11 relative (bf16 would cost 2^-8) -- the fp32-accumulated result stays
 // within 2e-3 of the exact attention even for rows with few keys.
@@ -168,7 +172,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
 struct Unit {
   int s, h0, q0, row0, rows, pos_first, ctx, n_kv;
   bool valid;      // rows to compute and consistent lengths
-  bool bad;        // rows but inconsistent lengths (reported, skipped)
+  bool bad;        // the sequence's lengths are inconsistent (reported, skipped)
   bool bad_ctx;    // the inconsistency is a context past the table's capacity
 };
 
@@ -206,8 +210,16 @@ __device__ __forceinline__ void unit_info(const Params& p, const int* tab, int u
   x.row0 = (p.n_qtiles - 1 - item % p.n_qtiles) * kBM;
   const int cap = p.max_blocks * p.bs;
   const bool rows_here = x.row0 < lq;
-  x.bad_ctx = x.ctx > cap;
-  x.bad = rows_here && (x.ctx < lq || x.bad_ctx);
+  // The whole sequence is skipped (and reported) when its query rows would
+  // leave [0, total_q) -- a negative or decreasing query_start_loc entry, or
+  // one past total_q_tokens -- when it has more rows than max_q_len's query
+  // tiles cover, or when its context cannot hold its chunk or exceeds the
+  // block table.  So no unit ever addresses a row outside `out`.
+  const bool bad_rows = x.q0 < 0 || lq < 0 ||
+                        static_cast<long long>(x.q0) + lq > static_cast<long long>(p.total_q) ||
+                        lq > p.n_qtiles * kBM;
+  x.bad_ctx = !bad_rows && x.ctx > cap;
+  x.bad = bad_rows || (lq > 0 && (x.ctx < lq || x.ctx > cap));
   x.valid = rows_here && !x.bad;
   x.rows = min(kBM, lq - x.row0);
   x.pos_first = x.ctx - lq + x.row0;
@@ -676,6 +688,19 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
                 make_float4(__uint_as_float(o[cc][e]) * inv, __uint_as_float(o[cc][e + 1]) * inv,
                             __uint_as_float(o[cc][e + 2]) * inv,
                             __uint_as_float(o[cc][e + 3]) * inv);
+        // A row that is not finite: a V value beyond the fp16 range of the
+        // P.V product (bf16 holds values past 65504), or non-finite inputs.
+        // The sum of the unnormalised row carries any inf or NaN.
+        float2 chk[4] = {};
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            chk[(e >> 1) & 3] = __fadd2_rn(chk[(e >> 1) & 3],
+                                           make_float2(__uint_as_float(o[cc][e]),
+                                                       __uint_as_float(o[cc][e + 1])));
+        const float2 c4 = __fadd2_rn(__fadd2_rn(chk[0], chk[1]), __fadd2_rn(chk[2], chk[3]));
+        if (!isfinite(c4.x + c4.y) || !isfinite(inv)) report(p.status, TVL_DEV_NONFINITE);
         fence_async_smem();
         bulk_store(p.out + (static_cast<long long>(x.q0 + x.row0 + r) * p.hq + x.h0 + hh) * kD,
                    stage, kD * 4);
@@ -685,7 +710,7 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
     }
     if (pending) bulk_wait_read();
     if (threadIdx.x == 0) {
-      // units with rows but inconsistent lengths were skipped: say so
+      // units of sequences with inconsistent lengths were skipped: say so
       for (int k = 0;; ++k) {
         const long long u = unit_index(k, c, G);
         if (u >= n_units) break;

@@ -84,11 +84,16 @@ def test_decode_continuous_batch(replica):
     assert_clean_status()
 
 
-@pytest.mark.parametrize("part", [512, 0])
-def test_decode_long_splitk(part):
-    wl = W.named("long_splitk", 0)
-    got, _ = gpu_decode(wl, partition_size=part)
-    assert_close(got, oracle_decode(wl), f"long P{part}")
+@pytest.mark.parametrize("replica", [0, 1, 2])
+def test_decode_long_splitk(replica):
+    """8 sequences of 32k-128k tokens: 512-token windows merged by
+    log-sum-exp, and the balanced split, on the same written cache."""
+    wl = W.named("long_splitk", replica)
+    ref = oracle_decode(wl)
+    got, t = gpu_decode(wl, partition_size=512)
+    assert_close(got, ref, f"long r{replica} P512")
+    got, _ = gpu_decode(wl, partition_size=0, write=False, tensors=t)
+    assert_close(got, ref, f"long r{replica} balanced")
     assert_clean_status()
 
 
@@ -205,9 +210,10 @@ def test_decode_workspace_too_small_is_rejected():
 
 @pytest.mark.parametrize("part", [0, 256])
 def test_decode_ignores_workspace_contents(part):
-    """The split-K tickets in the workspace are tagged per call, so a
-    workspace full of arbitrary bytes gives the same result as a zeroed one,
-    and reusing it for a second call changes nothing."""
+    """Every partial record the merge reads is written by the same call's
+    decode first, so a workspace full of arbitrary bytes gives the same
+    result as a zeroed one, and reusing it for a second call changes
+    nothing."""
     wl = W.make_decode(77, [5000, 17, 3000, 1, 700, 4096], num_q_heads=32, num_kv_heads=8,
                        block_size=16)
     t = W.to_device(wl, DEV)

@@ -68,14 +68,14 @@ def test_prefill_more_items_than_threads(hkv):
 
 
 @pytest.mark.parametrize("replica", [0, 1, 2])
-def test_prefill_chunked_config_sampled(replica):
+def test_prefill_chunked_config_every_row(replica):
+    """The full chunked-prefill batch (16 sequences, cached prefix U{0..2048}
+    + 512 new tokens, 32/8 heads, bs 16): every one of its 8192 x 32 output
+    rows against the oracle."""
     wl = W.named("chunked_prefill", replica)
     got, _ = gpu_prefill(wl)
-    gen = np.random.default_rng(replica)
-    mask = np.zeros(wl.total_q, dtype=np.uint8)
-    mask[gen.choice(wl.total_q, size=768, replace=False)] = 1
-    mask[int(wl.query_start_loc[0]):int(wl.query_start_loc[1])] = 1   # all of sequence 0
-    ref = oracle_prefill(wl, row_mask=mask)
+    ref = oracle_prefill(wl)
+    assert not np.isnan(ref).any()
     assert_close(got, ref, f"chunked r{replica}")
     assert np.isfinite(got).all()
     assert_clean_status()
@@ -158,6 +158,88 @@ def test_prefill_inconsistent_lengths_are_reported_and_skipped(hkv):
     ref = oracle_prefill(wl)
     assert_close(got[qsl[0]:qsl[1]], ref[qsl[0]:qsl[1]], "valid sequence")
     assert np.isnan(got[qsl[1]:qsl[3]]).all()
+    assert_clean_status()
+
+
+def test_prefill_bad_query_start_loc_is_reported_and_contained():
+    """query_start_loc entries that would put rows outside [0, Tq) -- a
+    decreasing entry, an end past total_q_tokens -- and a chunk longer than
+    max_q_len: those sequences are reported and skipped, nothing outside the
+    Tq rows of `out` is written (the buffer is allocated larger and its extra
+    rows must stay NaN), and the consistent sequence is computed as usual."""
+    wl = W.make_prefill(733, [30, 50, 70, 10], [40, 20, 30, 100], num_q_heads=8,
+                        num_kv_heads=2, block_size=16)
+    t = W.to_device(wl, DEV)
+    tvl.paged_kv_write(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["slot_mapping"])
+    tq = wl.total_q                                    # 190; the chunks start at 0, 40, 60, 90
+    # seq 1: [40, 30) decreasing; seq 2: [30, 180) has 150 rows, more than the
+    # 128 that max_q_len 100 provides; seq 3: [180, 190) is consistent -- the
+    # last 10 positions of its 110-token context, whose queries are rows
+    # 180..189 of q in the workload's own packing too.
+    qsl = torch.tensor([0, 40, 30, tq - 10, tq], dtype=torch.int32)
+    ctx = t["context_lens"].clone()
+    ref_rows = 40
+    extra = 64
+    out_big = torch.full((tq + extra, wl.num_q_heads, wl.head_dim), float("nan"),
+                         dtype=torch.float32, device=DEV)
+    out = out_big[:tq]
+    tvl.paged_attention_prefill(out, t["q"], qsl.to(DEV), t["k_cache"], t["v_cache"],
+                                t["block_tables"], ctx, wl.scale, 100)
+    torch.cuda.synchronize()
+    bits = tvl.get_device_status()
+    assert bits & tvl.DEV_BAD_QUERY_LEN
+    got = out_big.double().cpu().numpy()
+    assert np.isnan(got[tq:]).all(), "rows past total_q_tokens were written"
+    ref = oracle_prefill(wl)
+    assert_close(got[:ref_rows], ref[:ref_rows], "consistent sequence 0")
+    assert np.isnan(got[ref_rows:tq - 10]).all()
+    assert_close(got[tq - 10:tq], ref[tq - 10:tq], "consistent sequence 3")
+
+    # an end past total_q_tokens
+    qsl2 = torch.tensor([0, 40, 60, 90, tq + 5], dtype=torch.int32)
+    out_big.fill_(float("nan"))
+    tvl.paged_attention_prefill(out, t["q"], qsl2.to(DEV), t["k_cache"], t["v_cache"],
+                                t["block_tables"], ctx, wl.scale, 128)
+    torch.cuda.synchronize()
+    assert tvl.get_device_status() & tvl.DEV_BAD_QUERY_LEN
+    got = out_big.double().cpu().numpy()
+    assert np.isnan(got[tq:]).all(), "rows past total_q_tokens were written"
+    assert np.isnan(got[90:tq]).all()
+    assert_close(got[:90], ref[:90], "consistent sequences 0-2 (second call)")
+    assert_clean_status()
+
+
+def test_prefill_v_within_fp16_range():
+    """V entries of magnitude 3e4 (inside the fp16 range the P.V product
+    uses) give results as close to the oracle as N(0,1) ones, relative to
+    the largest |v|; nothing is reported."""
+    wl = W.make_prefill(734, [100, 0], [60, 130], num_q_heads=8, num_kv_heads=2, block_size=16)
+    vn = wl.v_new.float()
+    vn[5, 0, 3] = 30000.0
+    vn[70, 1, 10] = -30000.0
+    wl.v_new = vn.to(torch.bfloat16)
+    got, _ = gpu_prefill(wl)
+    ref = oracle_prefill(wl)
+    vmax = 30000.0
+    err = np.abs(got - ref)
+    assert np.isfinite(got).all()
+    assert err.max() <= MAX_ABS * vmax and err.mean() <= MEAN_ABS * vmax, (err.max(), err.mean())
+    assert_clean_status()
+
+
+def test_prefill_v_beyond_fp16_range_is_reported():
+    """A V value of 1e5 (a bf16 value beyond fp16's 65504) leaves output
+    rows that are not finite, which sets DEV_NONFINITE; a sequence whose keys
+    do not include it is unaffected."""
+    wl = W.make_prefill(735, [50, 20], [30, 40], num_q_heads=8, num_kv_heads=2, block_size=16)
+    vn = wl.v_new.float()
+    vn[45, 0, 7] = 1.0e5                              # a token of sequence 1
+    wl.v_new = vn.to(torch.bfloat16)
+    got, _ = gpu_prefill(wl)
+    bits = tvl.get_device_status()
+    assert bits & tvl.DEV_NONFINITE
+    ref = oracle_prefill(wl)
+    assert_close(got[:30], ref[:30], "sequence 0")
     assert_clean_status()
 
 
