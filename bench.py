@@ -396,7 +396,7 @@ def bench_decode(wl, args, world, device, decode_only=True):
     def run(i):
         steps[i % copies]()
 
-    args.warmup_run = warm_up(run, args.warmup)
+    args.warmup_run = warm_up(run, args.warmup, 0.0 if args.quick else 0.2)
     torch.cuda.synchronize(device)
     if tvl.get_device_status() != 0:
         raise RuntimeError("device status word set during warm-up")
@@ -406,6 +406,8 @@ def bench_decode(wl, args, world, device, decode_only=True):
     elapsed_ms = timed_region(run, args.steps, stream)
     if world > 1:
         torch.distributed.barrier()
+    if args.quick:
+        return {"elapsed_ms": elapsed_ms, "step_ms": elapsed_ms / args.steps, "copies": copies}
     sus_ms, clocks, sus_n = sustained_region(run, elapsed_ms / args.steps, stream, device)
 
     res = {"elapsed_ms": elapsed_ms, "step_ms": elapsed_ms / args.steps, "copies": copies,
@@ -527,10 +529,12 @@ def bench_prefill(wl, args, device):
         writes[i % copies]()
         prefills[i % copies]()
 
-    args.warmup_run = warm_up(step, args.warmup)
+    args.warmup_run = warm_up(step, args.warmup, 0.0 if args.quick else 0.2)
     torch.cuda.synchronize(device)
     elapsed = timed_region(step, args.steps, stream)
     kernel = timed_region(lambda i: prefills[i % copies](), args.steps, stream)
+    if args.quick:
+        return {"step_ms": elapsed / args.steps, "kernel_ms": kernel / args.steps}
     sus_ms, clocks, sus_n = sustained_region(lambda i: prefills[i % copies](),
                                              kernel / args.steps, stream, device)
     if tvl.get_device_status() != 0:
@@ -749,6 +753,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="print the selected workload only")
+    ap.add_argument("--quick", action="store_true",
+                    help="profiling runs: the W warm-up and K timed steps only (no sustained, "
+                         "decode-only or end-to-end regions, no CPU baseline, no extras); "
+                         "prints ms per step")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     args.steps = max(1, args.steps)
@@ -780,6 +788,14 @@ def main():
               "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic"}
 
     wl = rank_workload(args.config, rank)
+    if args.quick:
+        if args.config == "chunked_prefill":
+            r = bench_prefill(wl, args, device)
+        else:
+            r = bench_decode(wl, args, world, device, decode_only=False)
+        print(json.dumps({"quick": True, "workload": wl.name,
+                          **{k: round(v, 5) for k, v in r.items() if k.endswith("_ms")}}))
+        return
     if args.config == "chunked_prefill":
         if world > 1:
             raise SystemExit("the prefill line is measured on one GPU")
@@ -811,6 +827,25 @@ def main():
                       "synchronize; a ~0.2 ms GPU hold kernel (not timed) so "
                       "the host has queued the first steps; then exactly K steps back to back "
                       "between CUDA events on the launching stream; inputs larger than L2")
+    # Every GPU measurement first, the CPU-oracle samples last: the oracle's
+    # threads busy every host core, which must not overlap a timed region.
+    extras = {}
+    if world == 1 and args.config == "llama1b_decode" and not args.no_extras:
+        del r
+        torch.cuda.empty_cache()
+        for name in ("continuous_batch", "long_splitk"):
+            xw = W.named(name, 0)
+            xr = bench_decode(xw, args, 1, device, decode_only=False)
+            line[name] = decode_entry(xw, xr, hbm_peak, peak_src, f"decode_{name}.txt",
+                                      args.steps)
+            extras[name] = xw
+            del xr
+            torch.cuda.empty_cache()
+        pw = W.named("chunked_prefill", 0)
+        line["chunked_prefill"] = prefill_entry(pw, bench_prefill(pw, args, device), bf16_peak,
+                                                bf16_sus, peak_src, args.steps)
+        extras["chunked_prefill"] = pw
+
     if not args.no_cpu_baseline and world == 1:
         per, nbytes, cores, reps = cpu_baseline_decode(wl, budget_s=8.0)
         line["cpu_baseline"] = {
@@ -818,37 +853,26 @@ def main():
             "kind": "oracle",
             "sample": f"{reps} full steps (paged write + fp64 decode of all {wl.num_seqs} "
                       f"sequences), {per:.3f} s each; {cpu_model()}"}
-
-    if world == 1 and args.config == "llama1b_decode" and not args.no_extras:
-        del r
-        torch.cuda.empty_cache()
         for name in ("continuous_batch", "long_splitk"):
-            xw = W.named(name, 0)
-            xr = bench_decode(xw, args, 1, device, decode_only=False)
-            x = decode_entry(xw, xr, hbm_peak, peak_src, f"decode_{name}.txt", args.steps)
-            if not args.no_cpu_baseline:
-                seqs = None if name == "continuous_batch" else [0]
-                per, nbytes, cores, reps = cpu_baseline_decode(xw, budget_s=3.0, seqs=seqs)
-                what = (f"{reps} full steps (paged write + fp64 decode of all "
-                        f"{xw.num_seqs} sequences)" if seqs is None else
-                        f"{reps} fp64 decodes of sequence 0 alone "
-                        f"({int(xw.context_lens[0])} tokens; the write excluded)")
-                x["cpu_baseline"] = {"value": round(nbytes / per / 1e9, 3), "unit": "GB/s",
-                                     "cores": cores, "kind": "oracle",
-                                     "sample": f"{what}, {per:.3f} s each; {cpu_model()}"}
-            line[name] = x
-            del xw, xr
-            torch.cuda.empty_cache()
-        pw = W.named("chunked_prefill", 0)
-        p = prefill_entry(pw, bench_prefill(pw, args, device), bf16_peak, bf16_sus, peak_src,
-                          args.steps)
-        if not args.no_cpu_baseline:
-            sec, flops, cores = cpu_baseline_prefill(pw, every=32)
-            p["cpu_baseline"] = {"value": round(flops / sec / 1e12, 6), "unit": "TFLOP/s",
-                                 "cores": cores, "kind": "oracle",
-                                 "sample": f"fp64 prefill of every 32nd query row (all heads), "
-                                           f"{sec:.2f} s; {cpu_model()}"}
-        line["chunked_prefill"] = p
+            if name not in extras:
+                continue
+            xw = extras[name]
+            seqs = None if name == "continuous_batch" else [0]
+            per, nbytes, cores, reps = cpu_baseline_decode(xw, budget_s=3.0, seqs=seqs)
+            what = (f"{reps} full steps (paged write + fp64 decode of all "
+                    f"{xw.num_seqs} sequences)" if seqs is None else
+                    f"{reps} fp64 decodes of sequence 0 alone "
+                    f"({int(xw.context_lens[0])} tokens; the write excluded)")
+            line[name]["cpu_baseline"] = {"value": round(nbytes / per / 1e9, 3), "unit": "GB/s",
+                                          "cores": cores, "kind": "oracle",
+                                          "sample": f"{what}, {per:.3f} s each; {cpu_model()}"}
+        if "chunked_prefill" in extras:
+            sec, flops, cores = cpu_baseline_prefill(extras["chunked_prefill"], every=32)
+            line["chunked_prefill"]["cpu_baseline"] = {
+                "value": round(flops / sec / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+                "kind": "oracle",
+                "sample": f"fp64 prefill of every 32nd query row (all heads), {sec:.2f} s; "
+                          f"{cpu_model()}"}
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
