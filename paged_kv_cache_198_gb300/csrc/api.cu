@@ -292,7 +292,8 @@ tvl_status tvl_paged_attention_decode_workspace_size(int num_seqs, int num_q_hea
   tvl_status st = decode_sizes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                                block_size, partition_size, &records, &pb, &ms, &ctas);
   if (st != TVL_OK) return st;
-  *bytes = tvl::decode_workspace_bytes(records, num_q_heads, head_dim);
+  *bytes = tvl::decode_workspace_bytes(records, num_q_heads, head_dim,
+                                       tvl::decode_prefix_entries(num_seqs, pb));
   return TVL_OK;
 }
 
@@ -320,7 +321,8 @@ tvl_status decode_impl(float* out, const void* q, const void* k_new, const void*
     return fail(TVL_ERR_INVALID_ARG, "k_new and v_new must both be given");
   if ((k_new && !aligned16(k_new)) || (v_new && !aligned16(v_new)))
     return fail(TVL_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
-  const size_t need = tvl::decode_workspace_bytes(records, num_q_heads, head_dim);
+  const long long prefix = tvl::decode_prefix_entries(num_seqs, pb);
+  const size_t need = tvl::decode_workspace_bytes(records, num_q_heads, head_dim, prefix);
   if (need > 0) {
     if (!workspace || workspace_bytes < need)
       return fail(TVL_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", workspace_bytes, need);
@@ -349,7 +351,7 @@ tvl_status decode_impl(float* out, const void* q, const void* k_new, const void*
   a.partition_blocks = pb;
   a.max_splits = ms;
   a.balanced_ctas = ctas;
-  a.ws = tvl::decode_workspace_carve(workspace, records, num_q_heads, head_dim);
+  a.ws = tvl::decode_workspace_carve(workspace, records, num_q_heads, head_dim, prefix);
   a.status = word;
   cudaError_t e = tvl::launch_decode(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");

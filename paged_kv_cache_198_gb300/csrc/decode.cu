@@ -55,6 +55,8 @@
 // after its copies in flight have landed.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "device.cuh"
 #include "kernels.h"
 
@@ -226,14 +228,25 @@ __device__ void producer(const Params& p, const Schedule& sc, uint8_t* smem, con
   long long b = sc.block0;
   long long left = sc.count;
   bool first_seg = true;
+  // A window of 32 sequences: lane i holds the context length of sequence
+  // win_base + i and the ids of its first two blocks (those it has), so a
+  // segment that starts a sequence issues its first stage without waiting
+  // for a table load of its own -- with many short sequences that load was
+  // one memory round trip per sequence.
   int win_base = -1000000;
-  int win_ctx = 0;
+  int win_ctx = 0, win_t0 = 0, win_t1 = 0;
   while (ok && left > 0 && s < p.num_seqs) {
     if (s - win_base >= 32 || s < win_base) {
       win_base = s;
-      win_ctx = (s + lane < p.num_seqs) ? load_ctx(p, s + lane, BS) : 0;
+      const bool here = s + lane < p.num_seqs;
+      win_ctx = here ? load_ctx(p, s + lane, BS) : 0;
+      const int32_t* row = p.block_tables + static_cast<long long>(s + lane) * p.max_blocks;
+      win_t0 = here && win_ctx > 0 ? row[0] : 0;
+      win_t1 = here && win_ctx > BS && BS <= kStageTokens / 2 ? row[1] : 0;
     }
     const int ctx = __shfl_sync(kFull, win_ctx, s - win_base);
+    const int first0 = __shfl_sync(kFull, win_t0, s - win_base);
+    const int first1 = __shfl_sync(kFull, win_t1, s - win_base);
     const long long nb = (ctx + BS - 1) / BS;
     if (b >= nb) {
       ++s;
@@ -274,7 +287,11 @@ __device__ void producer(const Params& p, const Schedule& sc, uint8_t* smem, con
       for (long long blk = b; blk < e && ok; ++blk) {
         const int slot = static_cast<int>((blk - b) & 31);
         if (slot == 0) tbl = (blk + lane < e) ? table[blk + lane] : 0;
-        int phys = __shfl_sync(kFull, tbl, slot);
+        int phys;
+        if (blk == 0)
+          phys = first0;                                // from the window
+        else
+          phys = __shfl_sync(kFull, tbl, slot);
         bool phys_ok = true;
         if (phys < 0 || phys >= p.num_blocks) {
           if (lane == 0) report(p.status, TVL_DEV_BAD_BLOCK_ID);
@@ -356,7 +373,10 @@ __device__ void producer(const Params& p, const Schedule& sc, uint8_t* smem, con
       bool last_ok = true;                               // stage's last block id valid
 #pragma unroll
       for (int i = 0; i < BPS; ++i) {
-        phys[i] = __shfl_sync(kFull, tbl, slot + i);
+        if (blk == 0)                                    // the sequence's first stage
+          phys[i] = i == 0 ? first0 : first1;            // from the window
+        else
+          phys[i] = __shfl_sync(kFull, tbl, slot + i);
         if (i < nstage && (phys[i] < 0 || phys[i] >= p.num_blocks)) {
           if (lane == 0) report(p.status, TVL_DEV_BAD_BLOCK_ID);
           phys[i] = 0;
@@ -835,16 +855,23 @@ __global__ void __launch_bounds__((max_heads_per_cta(G) + 1) * 32, 1)
       for (int i = tid; i < p.hpc * G * kD; i += blockDim.x) p.out[base + i] = 0.f;
     }
   } else {
-    // balanced: this CTA streams flattened blocks [B*c/C, B*(c+1)/C)
+    // balanced: this CTA streams flattened blocks [B*c/C, B*(c+1)/C).  Each
+    // thread sums the block counts of a contiguous slice of the sequences,
+    // one block-wide scan gives every slice's first flattened block and the
+    // total B, and the thread whose slice holds block B*c/C walks it again
+    // to find the sequence and block this CTA starts at: O(S / threads)
+    // loads a thread and one scan, whatever the batch size.
     const int cta = blockIdx.x;
-    long long total = 0;
-    for (int base = 0; base < p.num_seqs; base += blockDim.x) {
-      const int s = base + tid;
-      const long long nb = s < p.num_seqs ? (load_ctx(p, s, BS) + BS - 1) / BS : 0;
-      long long incl, chunk_total;
-      block_scan(nb, incl, chunk_total, tmp);
-      total += chunk_total;
-    }
+    const int nthreads = static_cast<int>(blockDim.x);
+    const int per = (p.num_seqs + nthreads - 1) / nthreads;
+    const int s_lo = min(p.num_seqs, tid * per);
+    const int s_hi = min(p.num_seqs, s_lo + per);
+    long long mine = 0;
+#pragma unroll 4
+    for (int s = s_lo; s < s_hi; ++s) mine += (load_ctx(p, s, BS) + BS - 1) / BS;
+    long long incl, total;
+    block_scan(mine, incl, total, tmp);
+    const long long excl = incl - mine;
     const long long lo = total * cta / p.balanced_ctas;
     const long long hi = total * (cta + 1) / p.balanced_ctas;
     if (tid == 0) {
@@ -855,20 +882,27 @@ __global__ void __launch_bounds__((max_heads_per_cta(G) + 1) * 32, 1)
       sched->cta = cta;
     }
     __syncthreads();
-    long long run = 0;
-    if (hi > lo) {
-      for (int base = 0; base < p.num_seqs; base += blockDim.x) {
-        const int s = base + tid;
-        const long long nb = s < p.num_seqs ? (load_ctx(p, s, BS) + BS - 1) / BS : 0;
-        long long incl, chunk_total;
-        block_scan(nb, incl, chunk_total, tmp);
-        const long long excl = run + incl - nb;
-        if (nb > 0 && excl <= lo && lo < excl + nb) {
+    if (hi > lo && mine > 0 && excl <= lo && lo < excl + mine) {
+      long long run = excl;
+      for (int s = s_lo; s < s_hi; ++s) {
+        const long long nb = (load_ctx(p, s, BS) + BS - 1) / BS;
+        if (lo < run + nb) {
           sched->seq0 = s;
-          sched->block0 = static_cast<int>(lo - excl);
+          sched->block0 = static_cast<int>(lo - run);
+          break;
         }
-        run += chunk_total;
+        run += nb;
       }
+    }
+    // Large batches: the first flattened block of every sequence (and the
+    // total) for the merge, which then needs no scan of its own.
+    if (p.ws.seq_start != nullptr && cta == 0 && blockIdx.z == 0) {
+      long long run = excl;
+      for (int s = s_lo; s < s_hi; ++s) {
+        p.ws.seq_start[s] = run;
+        run += (load_ctx(p, s, BS) + BS - 1) / BS;
+      }
+      if (tid == 0) p.ws.seq_start[p.num_seqs] = total;
     }
   }
   __syncthreads();
@@ -895,6 +929,7 @@ constexpr int kMergeHeads = 4;       // query heads per CTA
 constexpr int kMergeMaxParts = 4;    // warps per head when sequences have many records
 constexpr int kMergeMaxRecords = 512; // record indices staged per pass
 constexpr int kMergeBatch = 16;       // records whose loads are in flight together
+constexpr int kMergeWalk = 128;       // split sequences a merge CTA lists at once
 
 __device__ __forceinline__ int merge_ctx(const MergeParams& p, int s) {
   int c = p.context_lens[s];
@@ -913,15 +948,17 @@ __global__ void __launch_bounds__(kMergeHeads * kMergeMaxParts * 32)
   __shared__ int recs[kMergeMaxRecords];
   __shared__ float part_m[kMergeMaxParts][kMergeHeads], part_l[kMergeMaxParts][kMergeHeads];
   __shared__ float part_o[kMergeMaxParts][kMergeHeads][kD];
-  const int s = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int parts = static_cast<int>(blockDim.x) / (32 * kMergeHeads);
   const int hw = warp % kMergeHeads, part = warp / kMergeHeads;
   const int h = blockIdx.y * kMergeHeads + hw;
+  // One sequence per CTA, except for large balanced batches (below).
+  auto merge_seq = [&](const int s) {
   const long long nb = (merge_ctx(p, s) + p.bs - 1) / p.bs;
   const bool fixed = p.partition_blocks > 0;
 
   long long n_cand = 0, seq_start = 0, total = 0, c_first = 0;
+  bool waited = false;
   if (fixed) {
     if (nb <= p.partition_blocks) return;   // single window: decode wrote the output
     n_cand = (nb + p.partition_blocks - 1) / p.partition_blocks;
@@ -935,17 +972,28 @@ __global__ void __launch_bounds__(kMergeHeads * kMergeMaxParts * 32)
       }
       return;
     }
-    long long tot_part = 0, pre_part = 0;
-    for (int i = tid; i < p.num_seqs; i += blockDim.x) {
-      const long long n = (merge_ctx(p, i) + p.bs - 1) / p.bs;
-      tot_part += n;
-      if (i < s) pre_part += n;
+    if (p.ws.seq_start != nullptr) {
+      // large batch: the decode recorded each sequence's first flattened
+      // block and the total (O(1) here instead of a scan of every length)
+      grid_dependency_wait();
+      waited = true;
+      seq_start = p.ws.seq_start[s];
+      total = p.ws.seq_start[p.num_seqs];
+    } else {
+      // small batch: scan the lengths here, before the dependency wait, so
+      // that this overlaps the decode's tail
+      long long tot_part = 0, pre_part = 0;
+      for (int i = tid; i < p.num_seqs; i += blockDim.x) {
+        const long long n = (merge_ctx(p, i) + p.bs - 1) / p.bs;
+        tot_part += n;
+        if (i < s) pre_part += n;
+      }
+      long long incl, all;
+      block_scan(tot_part, incl, all, tmp);
+      total = all;
+      block_scan(pre_part, incl, all, tmp);
+      seq_start = all;
     }
-    long long incl, all;
-    block_scan(tot_part, incl, all, tmp);
-    total = all;
-    block_scan(pre_part, incl, all, tmp);
-    seq_start = all;
     const long long C = p.balanced_ctas;
     c_first = balanced_cta_of(seq_start, total, C);
     const long long c_last = balanced_cta_of(seq_start + nb - 1, total, C);
@@ -966,11 +1014,10 @@ __global__ void __launch_bounds__(kMergeHeads * kMergeMaxParts * 32)
   };
 
   float mx = -INFINITY, den = 0.f, o0 = 0.f, o1 = 0.f;
-  bool waited = false;
   for (long long base = 0; base < n_cand; base += kMergeMaxRecords) {
     const int n = static_cast<int>(n_cand - base < kMergeMaxRecords ? n_cand - base
                                                                      : kMergeMaxRecords);
-    if (base > 0) __syncthreads();
+    __syncthreads();             // the previous pass (or sequence) has read recs
     for (int k = tid; k < n; k += blockDim.x) recs[k] = record_of(base + k);
     __syncthreads();
     if (!waited) {
@@ -1045,6 +1092,51 @@ __global__ void __launch_bounds__(kMergeHeads * kMergeMaxParts * 32)
   float* dst = p.out + (static_cast<long long>(s) * p.hq + h) * kD;
   dst[lane] = o0 * inv;
   dst[lane + 32] = o1 * inv;
+  };
+
+  if (p.ws.seq_start == nullptr) {     // one sequence per CTA
+    merge_seq(blockIdx.x);
+    return;
+  }
+  // Large balanced batch: this CTA owns sequences blockIdx.x + k gridDim.x.
+  // One thread per sequence finds, in parallel, those the decode split over
+  // several CTAs (from the recorded block offsets) and writes the zero rows
+  // of empty ones; then the CTA merges the split ones.  At most one split
+  // sequence per decode CTA boundary exists, and the round-robin ownership
+  // spreads them over the merge CTAs.
+  __shared__ int todo[kMergeWalk];
+  __shared__ int ntodo;
+  grid_dependency_wait();
+  const long long total = p.ws.seq_start[p.num_seqs];
+  const long long owned = (p.num_seqs - 1 - static_cast<long long>(blockIdx.x)) / gridDim.x + 1;
+  if (tid == 0) ntodo = 0;
+  __syncthreads();
+  for (long long k = tid; k < owned; k += blockDim.x) {
+    const int sq = static_cast<int>(blockIdx.x + k * gridDim.x);
+    const long long nb = (merge_ctx(p, sq) + p.bs - 1) / p.bs;
+    if (nb == 0) {
+      for (int hh = 0; hh < kMergeHeads; ++hh) {
+        const int hx = blockIdx.y * kMergeHeads + hh;
+        if (hx >= p.hq) break;
+        float4* dst = reinterpret_cast<float4*>(p.out + (static_cast<long long>(sq) * p.hq + hx) * kD);
+        for (int e = 0; e < kD / 4; ++e) dst[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    } else {
+      const long long st = p.ws.seq_start[sq];
+      if (balanced_cta_of(st, total, p.balanced_ctas) !=
+          balanced_cta_of(st + nb - 1, total, p.balanced_ctas)) {
+        const int slot = atomicAdd(&ntodo, 1);
+        if (slot < kMergeWalk) todo[slot] = sq;
+      }
+    }
+  }
+  __syncthreads();
+  const int n = ntodo;
+  if (n <= kMergeWalk) {
+    for (int i = 0; i < n; ++i) merge_seq(todo[i]);
+  } else {                             // more split sequences than the list holds
+    for (long long k = 0; k < owned; ++k) merge_seq(static_cast<int>(blockIdx.x + k * gridDim.x));
+  }
 }
 
 template <int G, int BS>
@@ -1063,6 +1155,10 @@ cudaError_t launch_t(const Params& prm, dim3 grid, uint32_t smem_bytes, cudaStre
 
 }  // namespace
 
+long long decode_prefix_entries(int num_seqs, int partition_blocks) {
+  return partition_blocks == 0 && num_seqs > kMergeScanMaxSeqs ? num_seqs + 1LL : 0LL;
+}
+
 long long decode_records(int num_seqs, int max_blocks_per_seq, int partition_blocks,
                          int balanced_ctas) {
   if (partition_blocks > 0) {
@@ -1072,24 +1168,30 @@ long long decode_records(int num_seqs, int max_blocks_per_seq, int partition_blo
   return 2LL * balanced_ctas;
 }
 
-size_t decode_workspace_bytes(long long records, int num_q_heads, int head_dim) {
+// Layout: m [rows], l [rows] (each padded to 256 bytes), acc [rows, D],
+// then the per-sequence block offsets (prefix_entries int64) of large
+// balanced batches.
+size_t decode_workspace_bytes(long long records, int num_q_heads, int head_dim,
+                              long long prefix_entries) {
   if (records <= 0) return 0;
   const size_t rows = static_cast<size_t>(records) * num_q_heads;
   const size_t a = (rows * sizeof(float) + 255) / 256 * 256;
-  return 2 * a + rows * head_dim * sizeof(float);
+  const size_t acc = (rows * head_dim * sizeof(float) + 255) / 256 * 256;
+  return 2 * a + acc + static_cast<size_t>(prefix_entries) * sizeof(long long);
 }
 
 DecodeWorkspace decode_workspace_carve(void* base, long long records, int num_q_heads,
-                                       int head_dim) {
-  DecodeWorkspace ws{nullptr, nullptr, nullptr};
+                                       int head_dim, long long prefix_entries) {
+  DecodeWorkspace ws{nullptr, nullptr, nullptr, nullptr};
   if (records <= 0 || base == nullptr) return ws;
   const size_t rows = static_cast<size_t>(records) * num_q_heads;
   const size_t a = (rows * sizeof(float) + 255) / 256 * 256;
+  const size_t acc = (rows * head_dim * sizeof(float) + 255) / 256 * 256;
   uint8_t* b = static_cast<uint8_t*>(base);
   ws.m = reinterpret_cast<float*>(b);
   ws.l = reinterpret_cast<float*>(b + a);
   ws.acc = reinterpret_cast<float*>(b + 2 * a);
-  (void)head_dim;
+  if (prefix_entries > 0) ws.seq_start = reinterpret_cast<long long*>(b + 2 * a + acc);
   return ws;
 }
 
@@ -1175,7 +1277,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   mp.balanced_ctas = a.balanced_ctas;
   mp.ws = a.ws;
   mp.status = a.status;
-  dim3 mgrid(a.num_seqs, (a.num_q_heads + kMergeHeads - 1) / kMergeHeads);
+  // large balanced batches: two CTAs per decode CTA, sequences dealt round-robin
+  const int mx = a.ws.seq_start != nullptr ? std::min(a.num_seqs, 2 * a.balanced_ctas)
+                                           : a.num_seqs;
+  dim3 mgrid(mx, (a.num_q_heads + kMergeHeads - 1) / kMergeHeads);
   // many records per sequence (fixed windows over long contexts): four warps
   // per head, each merging a quarter of the records
   const int parts = a.partition_blocks > 0 && a.max_splits > 64 ? kMergeMaxParts : 1;

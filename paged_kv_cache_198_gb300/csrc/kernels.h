@@ -71,10 +71,18 @@ cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream);
 // records; record r, query head h: m (log2 domain running max used),
 // l (sum of exp2), acc[D] (unnormalised weighted sum of V).
 struct DecodeWorkspace {
-  float* m;     // [records, Hq]
-  float* l;     // [records, Hq]
-  float* acc;   // [records, Hq, D]
+  float* m;               // [records, Hq]
+  float* l;               // [records, Hq]
+  float* acc;             // [records, Hq, D]
+  long long* seq_start;   // [S + 1] first flattened block of each sequence and
+                          // the total (balanced batches of more than
+                          // kMergeScanMaxSeqs sequences), else null
 };
+
+// Balanced batches up to this many sequences: every merge CTA scans the
+// context lengths itself (before its dependency wait); larger ones read the
+// offsets the decode wrote into the workspace.
+constexpr int kMergeScanMaxSeqs = 512;
 
 struct DecodeArgs {
   float* out;
@@ -98,10 +106,13 @@ struct DecodeArgs {
 // Number of workspace records the decode needs (0 = none).
 long long decode_records(int num_seqs, int max_blocks_per_seq, int partition_blocks,
                          int balanced_ctas);
+// int64 per-sequence offsets the workspace also holds (0 = none).
+long long decode_prefix_entries(int num_seqs, int partition_blocks);
 // Byte layout of the workspace for `records` records.
-size_t decode_workspace_bytes(long long records, int num_q_heads, int head_dim);
+size_t decode_workspace_bytes(long long records, int num_q_heads, int head_dim,
+                              long long prefix_entries);
 DecodeWorkspace decode_workspace_carve(void* base, long long records, int num_q_heads,
-                                       int head_dim);
+                                       int head_dim, long long prefix_entries);
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 

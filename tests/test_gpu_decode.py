@@ -139,6 +139,20 @@ def test_decode_many_short_sequences_balanced():
     assert_clean_status()
 
 
+@pytest.mark.parametrize("num_seqs,max_ctx", [(1500, 300), (4096, 64)])
+def test_decode_large_batches_balanced(num_seqs, max_ctx):
+    """Balanced batches beyond 512 sequences, where the merge reads the
+    per-sequence block offsets the decode recorded instead of scanning every
+    length: 1500 sequences of up to 300 tokens (many cut between CTAs) and
+    4096 short ones, against the oracle."""
+    gen = torch.Generator().manual_seed(num_seqs)
+    ctx = torch.randint(1, max_ctx + 1, (num_seqs,), generator=gen).tolist()
+    wl = W.make_decode(79 + num_seqs, ctx, num_q_heads=32, num_kv_heads=8, block_size=16)
+    got, _ = gpu_decode(wl, partition_size=0)
+    assert_close(got, oracle_decode(wl), f"{num_seqs} sequences")
+    assert_clean_status()
+
+
 # ------------------------------------------------------------------ invariants
 
 
