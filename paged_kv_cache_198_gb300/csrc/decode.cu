@@ -245,8 +245,7 @@ __device__ void producer(const Params& p, const Schedule& sc, uint8_t* smem, con
       win_t1 = here && win_ctx > BS && BS <= kStageTokens / 2 ? row[1] : 0;
     }
     const int ctx = __shfl_sync(kFull, win_ctx, s - win_base);
-    const int first0 = __shfl_sync(kFull, win_t0, s - win_base);
-    const int first1 = __shfl_sync(kFull, win_t1, s - win_base);
+    const int wl = s - win_base;                        // this sequence's window lane
     const long long nb = (ctx + BS - 1) / BS;
     if (b >= nb) {
       ++s;
@@ -289,7 +288,7 @@ __device__ void producer(const Params& p, const Schedule& sc, uint8_t* smem, con
         if (slot == 0) tbl = (blk + lane < e) ? table[blk + lane] : 0;
         int phys;
         if (blk == 0)
-          phys = first0;                                // from the window
+          phys = __shfl_sync(kFull, win_t0, wl);        // from the window
         else
           phys = __shfl_sync(kFull, tbl, slot);
         bool phys_ok = true;
@@ -373,8 +372,8 @@ __device__ void producer(const Params& p, const Schedule& sc, uint8_t* smem, con
       bool last_ok = true;                               // stage's last block id valid
 #pragma unroll
       for (int i = 0; i < BPS; ++i) {
-        if (blk == 0)                                    // the sequence's first stage
-          phys[i] = i == 0 ? first0 : first1;            // from the window
+        if (blk == 0)                                    // the sequence's first stage:
+          phys[i] = __shfl_sync(kFull, i == 0 ? win_t0 : win_t1, wl);   // from the window
         else
           phys[i] = __shfl_sync(kFull, tbl, slot + i);
         if (i < nstage && (phys[i] < 0 || phys[i] >= p.num_blocks)) {
@@ -855,54 +854,86 @@ __global__ void __launch_bounds__((max_heads_per_cta(G) + 1) * 32, 1)
       for (int i = tid; i < p.hpc * G * kD; i += blockDim.x) p.out[base + i] = 0.f;
     }
   } else {
-    // balanced: this CTA streams flattened blocks [B*c/C, B*(c+1)/C).  Each
-    // thread sums the block counts of a contiguous slice of the sequences,
-    // one block-wide scan gives every slice's first flattened block and the
-    // total B, and the thread whose slice holds block B*c/C walks it again
-    // to find the sequence and block this CTA starts at: O(S / threads)
-    // loads a thread and one scan, whatever the batch size.
+    // balanced: this CTA streams flattened blocks [B*c/C, B*(c+1)/C) of the
+    // B blocks of all sequences; the schedule is the sequence and block that
+    // flattened block B*c/C falls in.
     const int cta = blockIdx.x;
-    const int nthreads = static_cast<int>(blockDim.x);
-    const int per = (p.num_seqs + nthreads - 1) / nthreads;
-    const int s_lo = min(p.num_seqs, tid * per);
-    const int s_hi = min(p.num_seqs, s_lo + per);
-    long long mine = 0;
-#pragma unroll 4
-    for (int s = s_lo; s < s_hi; ++s) mine += (load_ctx(p, s, BS) + BS - 1) / BS;
-    long long incl, total;
-    block_scan(mine, incl, total, tmp);
-    const long long excl = incl - mine;
-    const long long lo = total * cta / p.balanced_ctas;
-    const long long hi = total * (cta + 1) / p.balanced_ctas;
-    if (tid == 0) {
-      sched->count = hi - lo;
-      sched->seq0 = p.num_seqs;
-      sched->block0 = 0;
-      sched->fixed_record = -1;
-      sched->cta = cta;
-    }
-    __syncthreads();
-    if (hi > lo && mine > 0 && excl <= lo && lo < excl + mine) {
-      long long run = excl;
-      for (int s = s_lo; s < s_hi; ++s) {
-        const long long nb = (load_ctx(p, s, BS) + BS - 1) / BS;
-        if (lo < run + nb) {
+    long long total = 0, lo = 0, hi = 0;
+    if (p.num_seqs <= static_cast<int>(blockDim.x) && p.ws.seq_start == nullptr) {
+      // a batch of at most one length per thread: a block-wide scan for the
+      // total, then a second one in which the thread of the sequence that
+      // holds block B*c/C records it
+      const int s = tid;
+      const long long nb = s < p.num_seqs ? (load_ctx(p, s, BS) + BS - 1) / BS : 0;
+      long long incl;
+      block_scan(nb, incl, total, tmp);
+      lo = total * cta / p.balanced_ctas;
+      hi = total * (cta + 1) / p.balanced_ctas;
+      if (tid == 0) {
+        sched->count = hi - lo;
+        sched->seq0 = p.num_seqs;
+        sched->block0 = 0;
+        sched->fixed_record = -1;
+        sched->cta = cta;
+      }
+      __syncthreads();
+      if (hi > lo) {
+        long long chunk_total;
+        block_scan(nb, incl, chunk_total, tmp);
+        const long long excl = incl - nb;
+        if (nb > 0 && excl <= lo && lo < excl + nb) {
           sched->seq0 = s;
-          sched->block0 = static_cast<int>(lo - run);
-          break;
+          sched->block0 = static_cast<int>(lo - excl);
         }
-        run += nb;
       }
-    }
-    // Large batches: the first flattened block of every sequence (and the
-    // total) for the merge, which then needs no scan of its own.
-    if (p.ws.seq_start != nullptr && cta == 0 && blockIdx.z == 0) {
-      long long run = excl;
-      for (int s = s_lo; s < s_hi; ++s) {
-        p.ws.seq_start[s] = run;
-        run += (load_ctx(p, s, BS) + BS - 1) / BS;
+    } else {
+      // larger batches: each thread sums the block counts of a contiguous
+      // slice of the sequences, one block-wide scan gives every slice's
+      // first flattened block and the total, and the thread whose slice
+      // holds block B*c/C walks it again to find the sequence and block:
+      // O(S / threads) loads a thread and one scan, whatever the batch size
+      const int nthreads = static_cast<int>(blockDim.x);
+      const int per = (p.num_seqs + nthreads - 1) / nthreads;
+      const int s_lo = min(p.num_seqs, tid * per);
+      const int s_hi = min(p.num_seqs, s_lo + per);
+      long long mine = 0;
+#pragma unroll 4
+      for (int s = s_lo; s < s_hi; ++s) mine += (load_ctx(p, s, BS) + BS - 1) / BS;
+      long long incl;
+      block_scan(mine, incl, total, tmp);
+      const long long excl = incl - mine;
+      lo = total * cta / p.balanced_ctas;
+      hi = total * (cta + 1) / p.balanced_ctas;
+      if (tid == 0) {
+        sched->count = hi - lo;
+        sched->seq0 = p.num_seqs;
+        sched->block0 = 0;
+        sched->fixed_record = -1;
+        sched->cta = cta;
       }
-      if (tid == 0) p.ws.seq_start[p.num_seqs] = total;
+      __syncthreads();
+      if (hi > lo && mine > 0 && excl <= lo && lo < excl + mine) {
+        long long run = excl;
+        for (int s = s_lo; s < s_hi; ++s) {
+          const long long nb = (load_ctx(p, s, BS) + BS - 1) / BS;
+          if (lo < run + nb) {
+            sched->seq0 = s;
+            sched->block0 = static_cast<int>(lo - run);
+            break;
+          }
+          run += nb;
+        }
+      }
+      // batches past kMergeScanMaxSeqs: the first flattened block of every
+      // sequence (and the total) for the merge, which then scans nothing
+      if (p.ws.seq_start != nullptr && cta == 0 && blockIdx.z == 0) {
+        long long run = excl;
+        for (int s = s_lo; s < s_hi; ++s) {
+          p.ws.seq_start[s] = run;
+          run += (load_ctx(p, s, BS) + BS - 1) / BS;
+        }
+        if (tid == 0) p.ws.seq_start[p.num_seqs] = total;
+      }
     }
   }
   __syncthreads();
@@ -929,7 +960,7 @@ constexpr int kMergeHeads = 4;       // query heads per CTA
 constexpr int kMergeMaxParts = 4;    // warps per head when sequences have many records
 constexpr int kMergeMaxRecords = 512; // record indices staged per pass
 constexpr int kMergeBatch = 16;       // records whose loads are in flight together
-constexpr int kMergeWalk = 128;       // split sequences a merge CTA lists at once
+constexpr int kMergeWalk = 256;       // split sequences a large-batch merge CTA lists at once
 
 __device__ __forceinline__ int merge_ctx(const MergeParams& p, int s) {
   int c = p.context_lens[s];
@@ -948,17 +979,15 @@ __global__ void __launch_bounds__(kMergeHeads * kMergeMaxParts * 32)
   __shared__ int recs[kMergeMaxRecords];
   __shared__ float part_m[kMergeMaxParts][kMergeHeads], part_l[kMergeMaxParts][kMergeHeads];
   __shared__ float part_o[kMergeMaxParts][kMergeHeads][kD];
+  const int s = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int parts = static_cast<int>(blockDim.x) / (32 * kMergeHeads);
   const int hw = warp % kMergeHeads, part = warp / kMergeHeads;
   const int h = blockIdx.y * kMergeHeads + hw;
-  // One sequence per CTA, except for large balanced batches (below).
-  auto merge_seq = [&](const int s) {
   const long long nb = (merge_ctx(p, s) + p.bs - 1) / p.bs;
   const bool fixed = p.partition_blocks > 0;
 
   long long n_cand = 0, seq_start = 0, total = 0, c_first = 0;
-  bool waited = false;
   if (fixed) {
     if (nb <= p.partition_blocks) return;   // single window: decode wrote the output
     n_cand = (nb + p.partition_blocks - 1) / p.partition_blocks;
@@ -972,28 +1001,17 @@ __global__ void __launch_bounds__(kMergeHeads * kMergeMaxParts * 32)
       }
       return;
     }
-    if (p.ws.seq_start != nullptr) {
-      // large batch: the decode recorded each sequence's first flattened
-      // block and the total (O(1) here instead of a scan of every length)
-      grid_dependency_wait();
-      waited = true;
-      seq_start = p.ws.seq_start[s];
-      total = p.ws.seq_start[p.num_seqs];
-    } else {
-      // small batch: scan the lengths here, before the dependency wait, so
-      // that this overlaps the decode's tail
-      long long tot_part = 0, pre_part = 0;
-      for (int i = tid; i < p.num_seqs; i += blockDim.x) {
-        const long long n = (merge_ctx(p, i) + p.bs - 1) / p.bs;
-        tot_part += n;
-        if (i < s) pre_part += n;
-      }
-      long long incl, all;
-      block_scan(tot_part, incl, all, tmp);
-      total = all;
-      block_scan(pre_part, incl, all, tmp);
-      seq_start = all;
+    long long tot_part = 0, pre_part = 0;
+    for (int i = tid; i < p.num_seqs; i += blockDim.x) {
+      const long long n = (merge_ctx(p, i) + p.bs - 1) / p.bs;
+      tot_part += n;
+      if (i < s) pre_part += n;
     }
+    long long incl, all;
+    block_scan(tot_part, incl, all, tmp);
+    total = all;
+    block_scan(pre_part, incl, all, tmp);
+    seq_start = all;
     const long long C = p.balanced_ctas;
     c_first = balanced_cta_of(seq_start, total, C);
     const long long c_last = balanced_cta_of(seq_start + nb - 1, total, C);
@@ -1014,10 +1032,11 @@ __global__ void __launch_bounds__(kMergeHeads * kMergeMaxParts * 32)
   };
 
   float mx = -INFINITY, den = 0.f, o0 = 0.f, o1 = 0.f;
+  bool waited = false;
   for (long long base = 0; base < n_cand; base += kMergeMaxRecords) {
     const int n = static_cast<int>(n_cand - base < kMergeMaxRecords ? n_cand - base
                                                                      : kMergeMaxRecords);
-    __syncthreads();             // the previous pass (or sequence) has read recs
+    if (base > 0) __syncthreads();
     for (int k = tid; k < n; k += blockDim.x) recs[k] = record_of(base + k);
     __syncthreads();
     if (!waited) {
@@ -1092,21 +1111,27 @@ __global__ void __launch_bounds__(kMergeHeads * kMergeMaxParts * 32)
   float* dst = p.out + (static_cast<long long>(s) * p.hq + h) * kD;
   dst[lane] = o0 * inv;
   dst[lane + 32] = o1 * inv;
-  };
+}
 
-  if (p.ws.seq_start == nullptr) {     // one sequence per CTA
-    merge_seq(blockIdx.x);
-    return;
-  }
-  // Large balanced batch: this CTA owns sequences blockIdx.x + k gridDim.x.
-  // One thread per sequence finds, in parallel, those the decode split over
-  // several CTAs (from the recorded block offsets) and writes the zero rows
-  // of empty ones; then the CTA merges the split ones.  At most one split
-  // sequence per decode CTA boundary exists, and the round-robin ownership
-  // spreads them over the merge CTAs.
+// Merge of a large balanced batch (more than kMergeScanMaxSeqs sequences):
+// the combination of merge_kernel, but the decode recorded each sequence's
+// first flattened block, so nothing scans the lengths.  The grid is two CTAs
+// per decode CTA (x) times the head groups (y), 4 warps (one per head); CTA
+// x owns sequences x + k gridDim.x.  One thread per sequence finds, in
+// parallel, those the decode split over several CTAs and writes the zero rows
+// of empty ones; then the CTA merges the split ones.  At most one split
+// sequence per decode CTA boundary exists, and the round-robin ownership
+// spreads them over the merge CTAs, so the kernel's time does not grow with
+// the batch.
+__global__ void __launch_bounds__(kMergeHeads * 32)
+    merge_walk_kernel(const MergeParams p) {
+  __shared__ int recs[kMergeMaxRecords];
   __shared__ int todo[kMergeWalk];
   __shared__ int ntodo;
-  grid_dependency_wait();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int h = blockIdx.y * kMergeHeads + warp;
+  const long long C = p.balanced_ctas;
+  grid_dependency_wait();              // the decode's records and block offsets
   const long long total = p.ws.seq_start[p.num_seqs];
   const long long owned = (p.num_seqs - 1 - static_cast<long long>(blockIdx.x)) / gridDim.x + 1;
   if (tid == 0) ntodo = 0;
@@ -1114,7 +1139,7 @@ __global__ void __launch_bounds__(kMergeHeads * kMergeMaxParts * 32)
   for (long long k = tid; k < owned; k += blockDim.x) {
     const int sq = static_cast<int>(blockIdx.x + k * gridDim.x);
     const long long nb = (merge_ctx(p, sq) + p.bs - 1) / p.bs;
-    if (nb == 0) {
+    if (nb == 0) {                     // empty context: zero rows
       for (int hh = 0; hh < kMergeHeads; ++hh) {
         const int hx = blockIdx.y * kMergeHeads + hh;
         if (hx >= p.hq) break;
@@ -1123,19 +1148,81 @@ __global__ void __launch_bounds__(kMergeHeads * kMergeMaxParts * 32)
       }
     } else {
       const long long st = p.ws.seq_start[sq];
-      if (balanced_cta_of(st, total, p.balanced_ctas) !=
-          balanced_cta_of(st + nb - 1, total, p.balanced_ctas)) {
+      if (balanced_cta_of(st, total, C) != balanced_cta_of(st + nb - 1, total, C)) {
         const int slot = atomicAdd(&ntodo, 1);
         if (slot < kMergeWalk) todo[slot] = sq;
       }
     }
   }
   __syncthreads();
-  const int n = ntodo;
-  if (n <= kMergeWalk) {
-    for (int i = 0; i < n; ++i) merge_seq(todo[i]);
-  } else {                             // more split sequences than the list holds
-    for (long long k = 0; k < owned; ++k) merge_seq(static_cast<int>(blockIdx.x + k * gridDim.x));
+  const int listed = ntodo;
+  // with more split sequences than the list holds (only with more than
+  // kMergeWalk decode CTAs), every owned sequence is visited
+  const long long n_seq = listed <= kMergeWalk ? listed : owned;
+  for (long long i = 0; i < n_seq; ++i) {
+    const int s = listed <= kMergeWalk ? todo[i] : static_cast<int>(blockIdx.x + i * gridDim.x);
+    const long long nb = (merge_ctx(p, s) + p.bs - 1) / p.bs;
+    if (nb == 0) continue;
+    const long long seq_start = p.ws.seq_start[s];
+    const long long c_first = balanced_cta_of(seq_start, total, C);
+    const long long c_last = balanced_cta_of(seq_start + nb - 1, total, C);
+    if (c_first == c_last) continue;   // one CTA held the whole sequence
+    const long long n_cand = c_last - c_first + 1;
+    float mx = -INFINITY, den = 0.f, o0 = 0.f, o1 = 0.f;
+    for (long long base = 0; base < n_cand; base += kMergeMaxRecords) {
+      const int n = static_cast<int>(n_cand - base < kMergeMaxRecords ? n_cand - base
+                                                                       : kMergeMaxRecords);
+      __syncthreads();                 // the previous pass (or sequence) has read recs
+      for (int k = tid; k < n; k += blockDim.x) {
+        // record of candidate CTA c, or -1 when it holds none of s
+        const long long c = c_first + base + k;
+        const long long lo = total * c / C, hi = total * (c + 1) / C;
+        const long long a = lo > seq_start ? lo : seq_start;
+        const long long b = hi < seq_start + nb ? hi : seq_start + nb;
+        recs[k] = a >= b ? -1 : static_cast<int>(2 * c + (seq_start <= lo ? 0 : 1));
+      }
+      __syncthreads();
+      if (h >= p.hq) continue;
+      for (int k0 = 0; k0 < n; k0 += kMergeBatch) {
+        float mv[kMergeBatch], lv[kMergeBatch], a0[kMergeBatch], a1[kMergeBatch];
+        bool have[kMergeBatch];
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+          const int r = k0 + u < n ? recs[k0 + u] : -1;
+          have[u] = r >= 0;
+          mv[u] = -INFINITY;
+          lv[u] = a0[u] = a1[u] = 0.f;
+          if (have[u]) {
+            const long long row = static_cast<long long>(r) * p.hq + h;
+            mv[u] = p.ws.m[row];
+            lv[u] = p.ws.l[row];
+            a0[u] = p.ws.acc[row * kD + lane];
+            a1[u] = p.ws.acc[row * kD + lane + 32];
+          }
+        }
+        float mb = mx;
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) mb = fmaxf(mb, mv[u]);
+        if (mb == -INFINITY) continue;
+        const float f = ex2(mx - mb);
+        den *= f;
+        o0 *= f;
+        o1 *= f;
+        mx = mb;
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+          const float wgt = have[u] ? ex2(mv[u] - mx) : 0.f;
+          den = fmaf(wgt, lv[u], den);
+          o0 = fmaf(wgt, a0[u], o0);
+          o1 = fmaf(wgt, a1[u], o1);
+        }
+      }
+    }
+    if (h >= p.hq) continue;
+    const float inv = 1.0f / den;
+    float* dst = p.out + (static_cast<long long>(s) * p.hq + h) * kD;
+    dst[lane] = o0 * inv;
+    dst[lane + 32] = o1 * inv;
   }
 }
 
@@ -1277,10 +1364,12 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   mp.balanced_ctas = a.balanced_ctas;
   mp.ws = a.ws;
   mp.status = a.status;
-  // large balanced batches: two CTAs per decode CTA, sequences dealt round-robin
-  const int mx = a.ws.seq_start != nullptr ? std::min(a.num_seqs, 2 * a.balanced_ctas)
-                                           : a.num_seqs;
-  dim3 mgrid(mx, (a.num_q_heads + kMergeHeads - 1) / kMergeHeads);
+  const unsigned hgroups = (a.num_q_heads + kMergeHeads - 1) / kMergeHeads;
+  if (a.ws.seq_start != nullptr)        // large balanced batch
+    return launch_pdl(merge_walk_kernel,
+                      dim3(std::min(a.num_seqs, 2 * a.balanced_ctas), hgroups),
+                      dim3(kMergeHeads * 32), 0, stream, mp);
+  dim3 mgrid(a.num_seqs, hgroups);
   // many records per sequence (fixed windows over long contexts): four warps
   // per head, each merging a quarter of the records
   const int parts = a.partition_blocks > 0 && a.max_splits > 64 ? kMergeMaxParts : 1;
