@@ -860,31 +860,38 @@ __global__ void __launch_bounds__((max_heads_per_cta(G) + 1) * 32, 1)
     const int cta = blockIdx.x;
     long long total = 0, lo = 0, hi = 0;
     if (p.num_seqs <= static_cast<int>(blockDim.x) && p.ws.seq_start == nullptr) {
-      // a batch of at most one length per thread: a block-wide scan for the
-      // total, then a second one in which the thread of the sequence that
-      // holds block B*c/C records it
+      // a batch of at most one length per thread: one block-wide scan gives
+      // the total and every sequence's first flattened block; the thread of
+      // the sequence that holds block B*c/C records it, and every thread
+      // whose sequence overlaps the CTA's range prefetches those table
+      // entries into L1 for the producer
       const int s = tid;
       const long long nb = s < p.num_seqs ? (load_ctx(p, s, BS) + BS - 1) / BS : 0;
       long long incl;
       block_scan(nb, incl, total, tmp);
       lo = total * cta / p.balanced_ctas;
       hi = total * (cta + 1) / p.balanced_ctas;
+      const long long excl = incl - nb;
       if (tid == 0) {
         sched->count = hi - lo;
-        sched->seq0 = p.num_seqs;
-        sched->block0 = 0;
         sched->fixed_record = -1;
         sched->cta = cta;
       }
-      __syncthreads();
-      if (hi > lo) {
-        long long chunk_total;
-        block_scan(nb, incl, chunk_total, tmp);
-        const long long excl = incl - nb;
-        if (nb > 0 && excl <= lo && lo < excl + nb) {
-          sched->seq0 = s;
-          sched->block0 = static_cast<int>(lo - excl);
-        }
+      if (hi <= lo && tid == 0) {
+        sched->seq0 = p.num_seqs;
+        sched->block0 = 0;
+      }
+      if (hi > lo && nb > 0 && excl <= lo && lo < excl + nb) {
+        sched->seq0 = s;
+        sched->block0 = static_cast<int>(lo - excl);
+      }
+      const long long a = lo > excl ? lo : excl;
+      const long long b = hi < excl + nb ? hi : excl + nb;
+      if (a < b) {
+        const int32_t* row = p.block_tables + static_cast<long long>(s) * p.max_blocks;
+        for (long long x = a - excl; x < b - excl; x += 32)
+          asm volatile("prefetch.global.L1 [%0];" ::"l"(row + x));
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(row + (b - excl - 1)));
       }
     } else {
       // larger batches: each thread sums the block counts of a contiguous
