@@ -684,47 +684,68 @@ __device__ __forceinline__ void process_stage(ConsumerState<G>& st, const uint8_
   }
 }
 
+// Ends a segment: the lanes' partial outputs are summed over the four token
+// groups and stored, normalised (record < 0) or as a partial record.  The
+// sum is a transposing reduction: a lane's 8G values form one flat array
+// (index (4h + k) * 2 + component); across the xor-16 pair each lane keeps
+// one half and sends the other, across the xor-8 pair one quarter, so token
+// group tg ends with the flat indices [2G tg, 2G (tg + 1)) summed -- 6G
+// shuffles instead of 16G, and the lanes of one dim chunk hold disjoint
+// parts of the output.
 template <int G>
 __device__ __forceinline__ void finish_segment(ConsumerState<G>& st, const Params& p, int seq,
                                                int record, int hq0) {
   using M = LaneMap<G>;
   const int lane = threadIdx.x & 31;
   const int c = lane & 7, tg = lane >> 3;
+  constexpr int V = 8 * G;                      // values a lane holds
+  constexpr int Q = V / 4;                      // values a lane keeps
   const float lt = reduce_sum_head<G>(st.l_part);
+  float a[V];
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
+  for (int h = 0; h < G; ++h)
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      float2 a = st.acc[h][k];
-      a.x += __shfl_xor_sync(kFull, a.x, 8);
-      a.y += __shfl_xor_sync(kFull, a.y, 8);
-      a.x += __shfl_xor_sync(kFull, a.x, 16);
-      a.y += __shfl_xor_sync(kFull, a.y, 16);
-      st.acc[h][k] = a;
+      a[(4 * h + k) * 2] = st.acc[h][k].x;
+      a[(4 * h + k) * 2 + 1] = st.acc[h][k].y;
     }
+  const bool hi2 = (tg & 2) != 0, hi1 = (tg & 1) != 0;
+#pragma unroll
+  for (int i = 0; i < V / 2; ++i) {
+    const float send = hi2 ? a[i] : a[i + V / 2];
+    const float keep = hi2 ? a[i + V / 2] : a[i];
+    a[i] = keep + __shfl_xor_sync(kFull, send, 16);
   }
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
+  for (int i = 0; i < Q; ++i) {
+    const float send = hi1 ? a[i] : a[i + Q];
+    const float keep = hi1 ? a[i + Q] : a[i];
+    a[i] = keep + __shfl_xor_sync(kFull, send, 8);
+  }
+  // a[i] is flat index Q * tg + i: head (Q tg + i) / 8, dim 8c + (Q tg + i) % 8
+  constexpr int HL = Q >= 8 ? Q / 8 : 1;        // heads this lane holds
+  constexpr int W = Q >= 8 ? 8 : Q;             // values per held head
+#pragma unroll
+  for (int j = 0; j < HL; ++j) {
+    const int h = (Q * tg) / 8 + j;
+    const int d0 = 8 * c + (Q >= 8 ? 0 : (Q * tg) % 8);
     const float lh = __shfl_sync(kFull, lt, tg * 8 + M::src_c(h));
     const float mh = __shfl_sync(kFull, st.m_used, tg * 8 + M::src_c(h));
-    if ((h & 3) == tg) {
-      const long long row = static_cast<long long>(record < 0 ? seq : record) * p.hq + hq0 + h;
-      if (record < 0) {
-        const float inv = 1.0f / lh;
-        float4* dst = reinterpret_cast<float4*>(p.out + row * kD + c * 8);
-        dst[0] = make_float4(st.acc[h][0].x * inv, st.acc[h][0].y * inv, st.acc[h][1].x * inv,
-                             st.acc[h][1].y * inv);
-        dst[1] = make_float4(st.acc[h][2].x * inv, st.acc[h][2].y * inv, st.acc[h][3].x * inv,
-                             st.acc[h][3].y * inv);
-      } else {
-        float4* dst = reinterpret_cast<float4*>(p.ws.acc + row * kD + c * 8);
-        dst[0] = make_float4(st.acc[h][0].x, st.acc[h][0].y, st.acc[h][1].x, st.acc[h][1].y);
-        dst[1] = make_float4(st.acc[h][2].x, st.acc[h][2].y, st.acc[h][3].x, st.acc[h][3].y);
-        if (c == 0) {
-          p.ws.m[row] = mh;
-          p.ws.l[row] = lh;
-        }
-      }
+    const long long row = static_cast<long long>(record < 0 ? seq : record) * p.hq + hq0 + h;
+    const float sc = record < 0 ? 1.0f / lh : 1.0f;
+    float* dst = (record < 0 ? p.out : p.ws.acc) + row * kD + d0;
+    const float* v = a + j * W;
+    if constexpr (W == 8) {
+      reinterpret_cast<float4*>(dst)[0] = make_float4(v[0] * sc, v[1] * sc, v[2] * sc, v[3] * sc);
+      reinterpret_cast<float4*>(dst)[1] = make_float4(v[4] * sc, v[5] * sc, v[6] * sc, v[7] * sc);
+    } else if constexpr (W == 4) {
+      reinterpret_cast<float4*>(dst)[0] = make_float4(v[0] * sc, v[1] * sc, v[2] * sc, v[3] * sc);
+    } else {
+      reinterpret_cast<float2*>(dst)[0] = make_float2(v[0] * sc, v[1] * sc);
+    }
+    if (record >= 0 && c == 0 && (Q >= 8 || (Q * tg) % 8 == 0)) {
+      p.ws.m[row] = mh;
+      p.ws.l[row] = lh;
     }
   }
 }
