@@ -12,8 +12,10 @@
 // Work split.  The context of every sequence is cut on physical-block
 // boundaries into segments:
 //   * balanced mode (partition_size 0): the flattened list of all sequences'
-//     blocks is divided evenly over one CTA per SM (per KV-head group), so
-//     each CTA streams the same number of blocks whatever the length mix;
+//     blocks is divided evenly over one CTA per SM (per KV-head group), each
+//     sequence start counted as one stage's worth of blocks more (it costs a
+//     CTA that much), so each CTA streams about the same time's worth of
+//     blocks whatever the length mix;
 //   * fixed mode (partition_size P): windows of P tokens from position 0,
 //     one CTA each.
 // A segment that covers its whole sequence writes the final output; any other
@@ -105,6 +107,7 @@ struct Params {
   int partition_blocks;  // fixed mode when > 0
   int max_splits;
   int balanced_ctas;
+  int seg_weight;        // balanced mode: cost of a sequence start, in blocks
   DecodeWorkspace ws;
   uint32_t* status;
 };
@@ -178,17 +181,27 @@ __device__ void block_scan(long long v, long long& incl, long long& total, long 
   __syncthreads();
 }
 
-// First CTA of the balanced split whose block range [B*c/C, B*(c+1)/C)
-// contains flattened block x (the largest c with B*c/C <= x).
+// The balanced split cuts a cost line into C equal ranges [T*c/C,
+// T*(c+1)/C).  On that line every sequence with blocks occupies w + nb
+// units: w for its start, then one per block (an empty sequence occupies
+// none).  A sequence start costs a CTA about one stage -- a partly filled
+// stage at the previous segment's end, the segment's reduction and store,
+// the next q -- so w is one stage's worth of blocks, and a CTA that takes
+// on sequence starts gets correspondingly fewer blocks.
+__host__ __device__ inline long long seq_cost(long long nb, int w) { return nb > 0 ? nb + w : 0; }
+
+// The CTA of the balanced split whose range contains position x of the cost
+// line (the largest c with T*c/C <= x).
 __host__ __device__ inline long long balanced_cta_of(long long x, long long total, long long ctas) {
   return ((x + 1) * ctas - 1) / total;
 }
 
 // Per-CTA schedule written to shared memory by the whole CTA.
 struct Schedule {
-  long long count;     // blocks to stream
   int seq0;            // first sequence
   int block0;          // first block inside it
+  int seq_end;         // streaming stops at block block_end of sequence
+  int block_end;       //   seq_end (seq_end == num_seqs: at the batch's end)
   int fixed_record;    // fixed mode: record of the single segment (-1: final)
   int cta;             // balanced mode: CTA index inside the KV-head group
 };
@@ -226,7 +239,6 @@ __device__ void producer(const Params& p, const Schedule& sc, uint8_t* smem, con
 
   int s = sc.seq0;
   long long b = sc.block0;
-  long long left = sc.count;
   bool first_seg = true;
   // A window of 32 sequences: lane i holds the context length of sequence
   // win_base + i and the ids of its first two blocks (those it has), so a
@@ -235,7 +247,7 @@ __device__ void producer(const Params& p, const Schedule& sc, uint8_t* smem, con
   // one memory round trip per sequence.
   int win_base = -1000000;
   int win_ctx = 0, win_t0 = 0, win_t1 = 0;
-  while (ok && left > 0 && s < p.num_seqs) {
+  while (ok && s < p.num_seqs && (s < sc.seq_end || (s == sc.seq_end && b < sc.block_end))) {
     if (s - win_base >= 32 || s < win_base) {
       win_base = s;
       const bool here = s + lane < p.num_seqs;
@@ -252,7 +264,7 @@ __device__ void producer(const Params& p, const Schedule& sc, uint8_t* smem, con
       b = 0;
       continue;
     }
-    const long long e = (nb < b + left) ? nb : b + left;
+    const long long e = (s == sc.seq_end && sc.block_end < nb) ? sc.block_end : nb;
     int record;
     if (fixed) {
       record = sc.fixed_record;
@@ -456,7 +468,6 @@ __device__ void producer(const Params& p, const Schedule& sc, uint8_t* smem, con
       }
       ++it;
     }
-    left -= e - b;
     first_seg = false;
     ++s;
     b = 0;
@@ -834,6 +845,143 @@ __device__ void consumer(const Params& p, uint8_t* smem, const Layout& L) {
 
 // ------------------------------------------------------------------ kernel
 
+// Schedule of a balanced CTA in a batch of more sequences than threads (or
+// when the merge wants every sequence's place): kept out of line so that its
+// code does not share the kernel body's instruction-cache footprint.
+template <int BS>
+__device__ __noinline__ void schedule_large(const Params& p, Schedule* sched, long long* tmp,
+                                            uint8_t* smem) {
+  const int tid = threadIdx.x;
+  const int cta = blockIdx.x;
+  const int w = p.seg_weight;
+  long long total = 0, lo = 0, hi = 0;
+  // larger batches: each thread sums the costs of a contiguous slice of
+  // the sequences, one block-wide scan gives every slice's place on the
+  // cost line and the total, and the threads whose slices hold positions
+  // T*c/C and T*(c+1)/C walk them again to find the sequence and block:
+  // O(S / threads) work a thread and one scan, whatever the batch size
+  const int nthreads = static_cast<int>(blockDim.x);
+  const int per = (p.num_seqs + nthreads - 1) / nthreads;
+  const int s_lo = min(p.num_seqs, tid * per);
+  const int s_hi = min(p.num_seqs, s_lo + per);
+  // Slices of more than 8 sequences: the costs are staged in the stage
+  // memory (idle until the producer starts) with coalesced loads, since a
+  // slice read straight from global memory makes every warp load touch 32
+  // cache lines, 8 of them in flight at a time.  Staged costs and in-slice
+  // offsets are 32-bit; batches whose figures could exceed that, or that do
+  // not fit, read global memory instead.
+  int32_t* cst_tab = reinterpret_cast<int32_t*>(smem);
+  const uint32_t tab_bytes = align_up(static_cast<uint32_t>(p.num_seqs) * 4u, 8u);
+  const bool staged =
+      per > 8 &&
+      static_cast<long long>(p.num_seqs) * 4 + 8LL * nthreads + 8 <=
+          static_cast<long long>(p.stages) * p.stage_bytes &&
+      static_cast<long long>(per) * (static_cast<long long>(p.max_blocks) + w) < (1LL << 31);
+  if (staged) {
+    // 8 coalesced lengths in flight per thread
+    for (int i0 = tid; i0 < p.num_seqs; i0 += 8 * nthreads) {
+      int c8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * nthreads;
+        c8[u] = i < p.num_seqs ? load_ctx(p, i, BS) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * nthreads;
+        if (i < p.num_seqs) cst_tab[i] = static_cast<int32_t>(seq_cost((c8[u] + BS - 1) / BS, w));
+      }
+    }
+    __syncthreads();
+  }
+  // the slice's costs 8 at a time (from global memory: 8 lengths in
+  // flight, one memory round trip per 8 sequences)
+  auto costs8 = [&](int s0, long long (&cst)[8]) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      cst[u] = s0 + u >= s_hi ? 0
+               : staged       ? static_cast<long long>(cst_tab[s0 + u])
+                              : seq_cost((load_ctx(p, s0 + u, BS) + BS - 1) / BS, w);
+  };
+  long long mine = 0;
+  for (int s0 = s_lo; s0 < s_hi; s0 += 8) {
+    long long cst[8];
+    costs8(s0, cst);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) mine += cst[u];
+  }
+  long long incl;
+  block_scan(mine, incl, total, tmp);
+  const long long excl = incl - mine;
+  lo = total * cta / p.balanced_ctas;
+  hi = total * (cta + 1) / p.balanced_ctas;
+  if (tid == 0) {
+    sched->seq0 = p.num_seqs;
+    sched->block0 = 0;
+    sched->seq_end = p.num_seqs;
+    sched->block_end = 0;
+    sched->fixed_record = -1;
+    sched->cta = cta;
+  }
+  __syncthreads();
+  // position x of the cost line -> (sequence, block), walking this slice
+  auto locate = [&](long long x, int& seq, int& blk) {
+    long long run = excl;
+    for (int s0 = s_lo; s0 < s_hi; s0 += 8) {
+      long long cst[8];
+      costs8(s0, cst);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (s0 + u < s_hi && x < run + cst[u]) {
+          seq = s0 + u;
+          blk = static_cast<int>(x - run - w > 0 ? x - run - w : 0);
+          return;
+        }
+        run += cst[u];
+      }
+    }
+  };
+  if (lo < total && mine > 0 && excl <= lo && lo < excl + mine)
+    locate(lo, sched->seq0, sched->block0);
+  if (hi < total && mine > 0 && excl <= hi && hi < excl + mine)
+    locate(hi, sched->seq_end, sched->block_end);
+  // batches past kMergeScanMaxSeqs: every sequence's place on the cost
+  // line (and the total) for the merge, which then scans nothing
+  if (p.ws.seq_start != nullptr && cta == 0 && blockIdx.z == 0) {
+    if (staged) {
+      // each slice's costs become offsets inside the slice (in place,
+      // after this thread's own walks); then one coalesced pass adds the
+      // slices' places and writes them out
+      long long* slice_at = reinterpret_cast<long long*>(smem + tab_bytes);
+      slice_at[tid] = excl;
+      int32_t run = 0;
+      for (int s2 = s_lo; s2 < s_hi; ++s2) {
+        const int32_t c2 = cst_tab[s2];
+        cst_tab[s2] = run;
+        run += c2;
+      }
+      __syncthreads();
+      for (int i = tid; i < p.num_seqs; i += nthreads)
+        p.ws.seq_start[i] = slice_at[i / per] + cst_tab[i];
+    } else {
+      long long run = excl;
+      for (int s0 = s_lo; s0 < s_hi; s0 += 8) {
+        long long cst[8];
+        costs8(s0, cst);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (s0 + u < s_hi) p.ws.seq_start[s0 + u] = run;
+          run += cst[u];
+        }
+      }
+    }
+    if (tid == 0) p.ws.seq_start[p.num_seqs] = total;
+  }
+  // the generic writes to the stage memory are ordered before the bulk
+  // copies (async proxy) that will fill it
+  if (staged) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 template <int G, int BS>
 __global__ void __launch_bounds__((max_heads_per_cta(G) + 1) * 32, 1)
     decode_kernel(const Params p) {
@@ -866,7 +1014,8 @@ __global__ void __launch_bounds__((max_heads_per_cta(G) + 1) * 32, 1)
       const long long nsplit = (nb + p.partition_blocks - 1) / p.partition_blocks;
       sched->seq0 = s;
       sched->block0 = static_cast<int>(b0);
-      sched->count = b0 < nb ? ((nb - b0) < p.partition_blocks ? nb - b0 : p.partition_blocks) : 0;
+      sched->seq_end = s;
+      sched->block_end = static_cast<int>(b0 < nb ? (nb - b0 < p.partition_blocks ? nb : b0 + p.partition_blocks) : b0);
       sched->fixed_record = nsplit <= 1 ? -1 : s * p.max_splits + win;
       sched->cta = win;
     }
@@ -875,93 +1024,56 @@ __global__ void __launch_bounds__((max_heads_per_cta(G) + 1) * 32, 1)
       for (int i = tid; i < p.hpc * G * kD; i += blockDim.x) p.out[base + i] = 0.f;
     }
   } else {
-    // balanced: this CTA streams flattened blocks [B*c/C, B*(c+1)/C) of the
-    // B blocks of all sequences; the schedule is the sequence and block that
-    // flattened block B*c/C falls in.
-    const int cta = blockIdx.x;
-    long long total = 0, lo = 0, hi = 0;
+    // balanced: this CTA streams the blocks in range [T*c/C, T*(c+1)/C) of
+    // the cost line (see seq_cost); the schedule is where that range's first
+    // and last blocks fall.
     if (p.num_seqs <= static_cast<int>(blockDim.x) && p.ws.seq_start == nullptr) {
+      const int cta = blockIdx.x;
+      const int w = p.seg_weight;
+      long long total = 0, lo = 0, hi = 0;
       // a batch of at most one length per thread: one block-wide scan gives
-      // the total and every sequence's first flattened block; the thread of
-      // the sequence that holds block B*c/C records it, and every thread
-      // whose sequence overlaps the CTA's range prefetches those table
-      // entries into L1 for the producer
+      // the total and every sequence's place on the cost line; the threads
+      // of the sequences holding positions T*c/C and T*(c+1)/C record them,
+      // and every thread whose sequence has blocks in the CTA's range
+      // prefetches those table entries into L1 for the producer
       const int s = tid;
       const long long nb = s < p.num_seqs ? (load_ctx(p, s, BS) + BS - 1) / BS : 0;
+      const long long cost = seq_cost(nb, w);
       long long incl;
-      block_scan(nb, incl, total, tmp);
+      block_scan(cost, incl, total, tmp);
       lo = total * cta / p.balanced_ctas;
       hi = total * (cta + 1) / p.balanced_ctas;
-      const long long excl = incl - nb;
+      const long long excl = incl - cost;
       if (tid == 0) {
-        sched->count = hi - lo;
         sched->fixed_record = -1;
         sched->cta = cta;
+        if (lo >= total) {
+          sched->seq0 = p.num_seqs;
+          sched->block0 = 0;
+        }
+        if (hi >= total) {
+          sched->seq_end = p.num_seqs;
+          sched->block_end = 0;
+        }
       }
-      if (hi <= lo && tid == 0) {
-        sched->seq0 = p.num_seqs;
-        sched->block0 = 0;
-      }
-      if (hi > lo && nb > 0 && excl <= lo && lo < excl + nb) {
+      if (cost > 0 && excl <= lo && lo < excl + cost) {
         sched->seq0 = s;
-        sched->block0 = static_cast<int>(lo - excl);
+        sched->block0 = static_cast<int>(lo - excl - w > 0 ? lo - excl - w : 0);
       }
-      const long long a = lo > excl ? lo : excl;
-      const long long b = hi < excl + nb ? hi : excl + nb;
+      if (cost > 0 && excl <= hi && hi < excl + cost) {
+        sched->seq_end = s;
+        sched->block_end = static_cast<int>(hi - excl - w > 0 ? hi - excl - w : 0);
+      }
+      const long long a = lo > excl + w ? lo : excl + w;            // this sequence's
+      const long long b = hi < excl + w + nb ? hi : excl + w + nb;  // blocks in range
       if (a < b) {
         const int32_t* row = p.block_tables + static_cast<long long>(s) * p.max_blocks;
-        for (long long x = a - excl; x < b - excl; x += 32)
+        for (long long x = a - excl - w; x < b - excl - w; x += 32)
           asm volatile("prefetch.global.L1 [%0];" ::"l"(row + x));
-        asm volatile("prefetch.global.L1 [%0];" ::"l"(row + (b - excl - 1)));
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(row + (b - excl - w - 1)));
       }
     } else {
-      // larger batches: each thread sums the block counts of a contiguous
-      // slice of the sequences, one block-wide scan gives every slice's
-      // first flattened block and the total, and the thread whose slice
-      // holds block B*c/C walks it again to find the sequence and block:
-      // O(S / threads) loads a thread and one scan, whatever the batch size
-      const int nthreads = static_cast<int>(blockDim.x);
-      const int per = (p.num_seqs + nthreads - 1) / nthreads;
-      const int s_lo = min(p.num_seqs, tid * per);
-      const int s_hi = min(p.num_seqs, s_lo + per);
-      long long mine = 0;
-#pragma unroll 4
-      for (int s = s_lo; s < s_hi; ++s) mine += (load_ctx(p, s, BS) + BS - 1) / BS;
-      long long incl;
-      block_scan(mine, incl, total, tmp);
-      const long long excl = incl - mine;
-      lo = total * cta / p.balanced_ctas;
-      hi = total * (cta + 1) / p.balanced_ctas;
-      if (tid == 0) {
-        sched->count = hi - lo;
-        sched->seq0 = p.num_seqs;
-        sched->block0 = 0;
-        sched->fixed_record = -1;
-        sched->cta = cta;
-      }
-      __syncthreads();
-      if (hi > lo && mine > 0 && excl <= lo && lo < excl + mine) {
-        long long run = excl;
-        for (int s = s_lo; s < s_hi; ++s) {
-          const long long nb = (load_ctx(p, s, BS) + BS - 1) / BS;
-          if (lo < run + nb) {
-            sched->seq0 = s;
-            sched->block0 = static_cast<int>(lo - run);
-            break;
-          }
-          run += nb;
-        }
-      }
-      // batches past kMergeScanMaxSeqs: the first flattened block of every
-      // sequence (and the total) for the merge, which then scans nothing
-      if (p.ws.seq_start != nullptr && cta == 0 && blockIdx.z == 0) {
-        long long run = excl;
-        for (int s = s_lo; s < s_hi; ++s) {
-          p.ws.seq_start[s] = run;
-          run += (load_ctx(p, s, BS) + BS - 1) / BS;
-        }
-        if (tid == 0) p.ws.seq_start[p.num_seqs] = total;
-      }
+      schedule_large<BS>(p, sched, tmp, smem);
     }
   }
   __syncthreads();
@@ -979,7 +1091,7 @@ struct MergeParams {
   float* out;
   const int32_t* context_lens;
   int num_seqs, hq, max_blocks, bs;
-  int partition_blocks, max_splits, balanced_ctas;
+  int partition_blocks, max_splits, balanced_ctas, seg_weight;
   DecodeWorkspace ws;
   uint32_t* status;
 };
@@ -1029,9 +1141,10 @@ __global__ void __launch_bounds__(kMergeHeads * kMergeMaxParts * 32)
       }
       return;
     }
+    // the same cost line as the decode's split (see seq_cost)
     long long tot_part = 0, pre_part = 0;
     for (int i = tid; i < p.num_seqs; i += blockDim.x) {
-      const long long n = (merge_ctx(p, i) + p.bs - 1) / p.bs;
+      const long long n = seq_cost((merge_ctx(p, i) + p.bs - 1) / p.bs, p.seg_weight);
       tot_part += n;
       if (i < s) pre_part += n;
     }
@@ -1039,10 +1152,11 @@ __global__ void __launch_bounds__(kMergeHeads * kMergeMaxParts * 32)
     block_scan(tot_part, incl, all, tmp);
     total = all;
     block_scan(pre_part, incl, all, tmp);
-    seq_start = all;
+    seq_start = all;                   // this sequence's place; its blocks follow w later
     const long long C = p.balanced_ctas;
-    c_first = balanced_cta_of(seq_start, total, C);
-    const long long c_last = balanced_cta_of(seq_start + nb - 1, total, C);
+    const long long first = seq_start + p.seg_weight;
+    c_first = balanced_cta_of(first, total, C);
+    const long long c_last = balanced_cta_of(first + nb - 1, total, C);
     if (c_first == c_last) return;   // one CTA held the whole sequence
     n_cand = c_last - c_first + 1;
   }
@@ -1053,9 +1167,12 @@ __global__ void __launch_bounds__(kMergeHeads * kMergeMaxParts * 32)
     const long long c = c_first + k;
     const long long lo = total * c / p.balanced_ctas;
     const long long hi = total * (c + 1) / p.balanced_ctas;
-    const long long a = lo > seq_start ? lo : seq_start;
-    const long long b = hi < seq_start + nb ? hi : seq_start + nb;
+    const long long first = seq_start + p.seg_weight;
+    const long long a = lo > first ? lo : first;
+    const long long b = hi < first + nb ? hi : first + nb;
     if (a >= b) return -1;
+    // the CTA's first segment is this sequence when its range starts at or
+    // after the sequence's place on the line
     return static_cast<int>(2 * c + (seq_start <= lo ? 0 : 1));
   };
 
@@ -1175,8 +1292,8 @@ __global__ void __launch_bounds__(kMergeHeads * 32)
         for (int e = 0; e < kD / 4; ++e) dst[e] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     } else {
-      const long long st = p.ws.seq_start[sq];
-      if (balanced_cta_of(st, total, C) != balanced_cta_of(st + nb - 1, total, C)) {
+      const long long first = p.ws.seq_start[sq] + p.seg_weight;   // its first block's place
+      if (balanced_cta_of(first, total, C) != balanced_cta_of(first + nb - 1, total, C)) {
         const int slot = atomicAdd(&ntodo, 1);
         if (slot < kMergeWalk) todo[slot] = sq;
       }
@@ -1192,8 +1309,9 @@ __global__ void __launch_bounds__(kMergeHeads * 32)
     const long long nb = (merge_ctx(p, s) + p.bs - 1) / p.bs;
     if (nb == 0) continue;
     const long long seq_start = p.ws.seq_start[s];
-    const long long c_first = balanced_cta_of(seq_start, total, C);
-    const long long c_last = balanced_cta_of(seq_start + nb - 1, total, C);
+    const long long first = seq_start + p.seg_weight;
+    const long long c_first = balanced_cta_of(first, total, C);
+    const long long c_last = balanced_cta_of(first + nb - 1, total, C);
     if (c_first == c_last) continue;   // one CTA held the whole sequence
     const long long n_cand = c_last - c_first + 1;
     float mx = -INFINITY, den = 0.f, o0 = 0.f, o1 = 0.f;
@@ -1205,8 +1323,8 @@ __global__ void __launch_bounds__(kMergeHeads * 32)
         // record of candidate CTA c, or -1 when it holds none of s
         const long long c = c_first + base + k;
         const long long lo = total * c / C, hi = total * (c + 1) / C;
-        const long long a = lo > seq_start ? lo : seq_start;
-        const long long b = hi < seq_start + nb ? hi : seq_start + nb;
+        const long long a = lo > first ? lo : first;
+        const long long b = hi < first + nb ? hi : first + nb;
         recs[k] = a >= b ? -1 : static_cast<int>(2 * c + (seq_start <= lo ? 0 : 1));
       }
       __syncthreads();
@@ -1344,6 +1462,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   prm.partition_blocks = a.partition_blocks;
   prm.max_splits = a.max_splits;
   prm.balanced_ctas = a.balanced_ctas;
+  // a sequence start costs about one 32-token stage: 32 / bs blocks, rounded
+  prm.seg_weight = a.partition_blocks > 0 ? 0 : (kStageTokens + bs / 2) / bs;
   prm.ws = a.ws;
   prm.status = a.status;
   const uint32_t smem = make_layout(stages, prm.stage_bytes, hpc, G).total;
@@ -1390,6 +1510,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   mp.partition_blocks = a.partition_blocks;
   mp.max_splits = a.max_splits;
   mp.balanced_ctas = a.balanced_ctas;
+  mp.seg_weight = prm.seg_weight;
   mp.ws = a.ws;
   mp.status = a.status;
   const unsigned hgroups = (a.num_q_heads + kMergeHeads - 1) / kMergeHeads;

@@ -74,9 +74,10 @@ struct DecodeWorkspace {
   float* m;               // [records, Hq]
   float* l;               // [records, Hq]
   float* acc;             // [records, Hq, D]
-  long long* seq_start;   // [S + 1] first flattened block of each sequence and
-                          // the total (balanced batches of more than
-                          // kMergeScanMaxSeqs sequences), else null
+  long long* seq_start;   // [S + 1] each sequence's place on the balanced
+                          // split's cost line and the line's total (balanced
+                          // batches of more than kMergeScanMaxSeqs
+                          // sequences), else null
 };
 
 // Balanced batches up to this many sequences: every merge CTA scans the
