@@ -351,6 +351,13 @@ tvl_status decode_impl(float* out, const void* q, const void* k_new, const void*
   a.partition_blocks = pb;
   a.max_splits = ms;
   a.balanced_ctas = ctas;
+  a.window_ctas = 0;
+  if (pb > 0 && ms > 1) {   // several windows a sequence: one persistent CTA per SM
+    int sms = 0;
+    st = sm_count(&sms);
+    if (st != TVL_OK) return st;
+    a.window_ctas = balanced_ctas(sms, num_q_heads, num_kv_heads);
+  }
   a.ws = tvl::decode_workspace_carve(workspace, records, num_q_heads, head_dim, prefix);
   a.status = word;
   cudaError_t e = tvl::launch_decode(a, static_cast<cudaStream_t>(stream));

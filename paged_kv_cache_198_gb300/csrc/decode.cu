@@ -108,6 +108,7 @@ struct Params {
   int max_splits;
   int balanced_ctas;
   int seg_weight;        // balanced mode: cost of a sequence start, in blocks
+  int window_walk;       // fixed mode: a persistent grid walks the windows
   DecodeWorkspace ws;
   uint32_t* status;
 };
@@ -202,7 +203,6 @@ struct Schedule {
   int block0;          // first block inside it
   int seq_end;         // streaming stops at block block_end of sequence
   int block_end;       //   seq_end (seq_end == num_seqs: at the batch's end)
-  int fixed_record;    // fixed mode: record of the single segment (-1: final)
   int cta;             // balanced mode: CTA index inside the KV-head group
 };
 
@@ -264,10 +264,16 @@ __device__ void producer(const Params& p, const Schedule& sc, uint8_t* smem, con
       b = 0;
       continue;
     }
-    const long long e = (s == sc.seq_end && sc.block_end < nb) ? sc.block_end : nb;
+    long long e = (s == sc.seq_end && sc.block_end < nb) ? sc.block_end : nb;
     int record;
     if (fixed) {
-      record = sc.fixed_record;
+      // one segment per window: its record is (sequence, window), or none
+      // when the sequence has a single window
+      const long long win = b / p.partition_blocks;
+      const long long wend = (win + 1) * p.partition_blocks;
+      if (wend < e) e = wend;
+      record = nb <= p.partition_blocks ? -1
+                                        : static_cast<int>(s * static_cast<long long>(p.max_splits) + win);
     } else {
       record = (b == 0 && e == nb) ? -1 : 2 * sc.cta + (first_seg ? 0 : 1);
     }
@@ -469,8 +475,11 @@ __device__ void producer(const Params& p, const Schedule& sc, uint8_t* smem, con
       ++it;
     }
     first_seg = false;
-    ++s;
-    b = 0;
+    b = e;                 // the next window of this sequence, or the next sequence
+    if (b >= nb) {
+      ++s;
+      b = 0;
+    }
   }
   // Tell the consumers to stop.
   int st;
@@ -920,7 +929,6 @@ __device__ __noinline__ void schedule_large(const Params& p, Schedule* sched, lo
     sched->block0 = 0;
     sched->seq_end = p.num_seqs;
     sched->block_end = 0;
-    sched->fixed_record = -1;
     sched->cta = cta;
   }
   __syncthreads();
@@ -982,6 +990,58 @@ __device__ __noinline__ void schedule_large(const Params& p, Schedule* sched, lo
   if (staged) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Fixed windows walked by a persistent grid: the windows of all sequences,
+// in (sequence, window) order, are dealt to the C CTAs in equal contiguous
+// ranges; a CTA streams its windows one after the other (a segment and a
+// record each), so its copies run on across window boundaries instead of a
+// CTA starting, filling its ring and draining it for every window.  Out of
+// line, like schedule_large.
+template <int BS>
+__device__ __noinline__ void schedule_windows(const Params& p, Schedule* sched, long long* tmp) {
+  const int tid = threadIdx.x;
+  const int nthreads = static_cast<int>(blockDim.x);
+  const int cta = blockIdx.x;
+  const long long P = p.partition_blocks;
+  const int per = (p.num_seqs + nthreads - 1) / nthreads;
+  const int s_lo = min(p.num_seqs, tid * per);
+  const int s_hi = min(p.num_seqs, s_lo + per);
+  auto windows = [&](int s) -> long long {
+    return ((load_ctx(p, s, BS) + BS - 1) / BS + P - 1) / P;
+  };
+  long long mine = 0;
+  for (int s = s_lo; s < s_hi; ++s) mine += windows(s);
+  long long incl, total;
+  block_scan(mine, incl, total, tmp);
+  const long long excl = incl - mine;
+  const long long lo = total * cta / p.balanced_ctas;
+  const long long hi = total * (cta + 1) / p.balanced_ctas;
+  if (tid == 0) {
+    sched->seq0 = p.num_seqs;
+    sched->block0 = 0;
+    sched->seq_end = p.num_seqs;
+    sched->block_end = 0;
+    sched->cta = cta;
+  }
+  __syncthreads();
+  // window x of the walk -> (sequence, its first block), walking this slice
+  auto locate = [&](long long x, int& seq, int& blk) {
+    long long run = excl;
+    for (int s = s_lo; s < s_hi; ++s) {
+      const long long n = windows(s);
+      if (x < run + n) {
+        seq = s;
+        blk = static_cast<int>((x - run) * P);
+        return;
+      }
+      run += n;
+    }
+  };
+  if (lo < total && mine > 0 && excl <= lo && lo < excl + mine)
+    locate(lo, sched->seq0, sched->block0);
+  if (hi < total && mine > 0 && excl <= hi && hi < excl + mine)
+    locate(hi, sched->seq_end, sched->block_end);
+}
+
 template <int G, int BS>
 __global__ void __launch_bounds__((max_heads_per_cta(G) + 1) * 32, 1)
     decode_kernel(const Params p) {
@@ -1003,7 +1063,9 @@ __global__ void __launch_bounds__((max_heads_per_cta(G) + 1) * 32, 1)
   grid_dependency_wait();        // inputs may come from the preceding kernel
   grid_dependents_launch();
 
-  if (p.partition_blocks > 0) {
+  if (p.window_walk) {
+    schedule_windows<BS>(p, sched, tmp);
+  } else if (p.partition_blocks > 0) {
     // fixed windows: CTA (x = window, y = sequence)
     const int s = blockIdx.y;
     const int win = blockIdx.x;
@@ -1011,12 +1073,10 @@ __global__ void __launch_bounds__((max_heads_per_cta(G) + 1) * 32, 1)
     const long long nb = (ctx + BS - 1) / BS;
     const long long b0 = static_cast<long long>(win) * p.partition_blocks;
     if (tid == 0) {
-      const long long nsplit = (nb + p.partition_blocks - 1) / p.partition_blocks;
       sched->seq0 = s;
       sched->block0 = static_cast<int>(b0);
       sched->seq_end = s;
       sched->block_end = static_cast<int>(b0 < nb ? (nb - b0 < p.partition_blocks ? nb : b0 + p.partition_blocks) : b0);
-      sched->fixed_record = nsplit <= 1 ? -1 : s * p.max_splits + win;
       sched->cta = win;
     }
     if (nb == 0 && win == 0) {   // empty context: zero output rows
@@ -1045,7 +1105,6 @@ __global__ void __launch_bounds__((max_heads_per_cta(G) + 1) * 32, 1)
       hi = total * (cta + 1) / p.balanced_ctas;
       const long long excl = incl - cost;
       if (tid == 0) {
-        sched->fixed_record = -1;
         sched->cta = cta;
         if (lo >= total) {
           sched->seq0 = p.num_seqs;
@@ -1128,11 +1187,12 @@ __global__ void __launch_bounds__(kMergeHeads * kMergeMaxParts * 32)
   const bool fixed = p.partition_blocks > 0;
 
   long long n_cand = 0, seq_start = 0, total = 0, c_first = 0;
-  if (fixed) {
+  if (fixed && nb > 0) {
     if (nb <= p.partition_blocks) return;   // single window: decode wrote the output
     n_cand = (nb + p.partition_blocks - 1) / p.partition_blocks;
   } else {
-    if (nb == 0) {
+    if (nb == 0) {   // an empty context: zero rows (no decode CTA owns it in a
+                     // balanced batch or a window walk)
       grid_dependency_wait();
       if (h < p.hq && part == 0) {
         float* dst = p.out + (static_cast<long long>(s) * p.hq + h) * kD;
@@ -1464,12 +1524,18 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   prm.balanced_ctas = a.balanced_ctas;
   // a sequence start costs about one 32-token stage: 32 / bs blocks, rounded
   prm.seg_weight = a.partition_blocks > 0 ? 0 : (kStageTokens + bs / 2) / bs;
+  // more possible windows than persistent CTAs: the CTAs walk the windows
+  prm.window_walk = a.partition_blocks > 0 && a.window_ctas > 0 &&
+                    static_cast<long long>(a.max_splits) * a.num_seqs > a.window_ctas;
+  if (prm.window_walk) prm.balanced_ctas = a.window_ctas;
   prm.ws = a.ws;
   prm.status = a.status;
   const uint32_t smem = make_layout(stages, prm.stage_bytes, hpc, G).total;
 
   dim3 grid;
-  if (a.partition_blocks > 0)
+  if (prm.window_walk)
+    grid = dim3(a.window_ctas, 1, groups);
+  else if (a.partition_blocks > 0)
     grid = dim3(a.max_splits, a.num_seqs, groups);
   else
     grid = dim3(a.balanced_ctas, 1, groups);

@@ -100,6 +100,8 @@ struct DecodeArgs {
   int partition_blocks;   // > 0: fixed windows of this many blocks; 0: balanced
   int max_splits;         // fixed mode: ceil(MB / partition_blocks)
   int balanced_ctas;      // balanced mode: CTAs per KV-head group
+  int window_ctas;        // fixed mode: CTAs per KV-head group that walk the
+                          // windows persistently (0: one CTA per window)
   DecodeWorkspace ws;
   uint32_t* status;
 };
