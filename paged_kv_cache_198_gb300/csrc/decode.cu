@@ -17,7 +17,8 @@
 //     CTA that much), so each CTA streams about the same time's worth of
 //     blocks whatever the length mix;
 //   * fixed mode (partition_size P): windows of P tokens from position 0,
-//     one CTA each.
+//     a segment each; with more windows than SMs a persistent grid (one CTA
+//     per SM) walks them in equal contiguous ranges, else one CTA each.
 // A segment that covers its whole sequence writes the final output; any other
 // writes a partial (m, l, acc) record, and merge_kernel combines the records
 // of a sequence by log-sum-exp -- the associative form of the online softmax
