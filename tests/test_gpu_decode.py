@@ -114,6 +114,24 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (64, 8)])
+def test_decode_window_walk_with_empty_sequences(hq, hkv):
+    """More windows than SMs: a persistent grid walks the fixed windows, a
+    segment and a record each (the merge then zeroes the empty sequences,
+    which no CTA owns)."""
+    gen = np.random.default_rng(77)
+    ctx = [int(c) for c in gen.integers(0, 600, 300)]
+    for i in range(0, 300, 9):
+        ctx[i] = 0
+    wl = W.make_decode(777, ctx, num_q_heads=hq, num_kv_heads=hkv, block_size=16)
+    got, _ = gpu_decode(wl, partition_size=64)
+    ref = oracle_decode(wl)
+    assert_close(got, ref, f"window walk G{hq // hkv}")
+    zero = np.array(ctx) == 0
+    assert np.array_equal(got[zero], np.zeros_like(got[zero]))
+    assert_clean_status()
+
+
 @pytest.mark.parametrize("case", range(len(CASES)))
 @pytest.mark.parametrize("part", [0, 32, 256])
 def test_decode_random_shapes(case, part):

@@ -39,6 +39,9 @@ CASES = [
     ([129, 7, 3000, 0, 44], 16, 8, 32, 512),    # G = 2, an empty sequence
     ([1, 64, 65, 700, 2047], 32, 8, 64, 0),     # blocks of 64
     ([128, 129, 5, 1000], 64, 8, 128, 256),     # G = 8, blocks of 128, fixed windows
+    # more windows than SMs: the windows are walked by a persistent grid
+    ([0 if i % 7 == 0 else (i * 37) % 300 + 1 for i in range(200)], 32, 8, 16, 64),
+    ([0 if i % 5 == 0 else (i * 53) % 400 + 1 for i in range(120)], 64, 8, 16, 32),
 ]
 
 
