@@ -118,6 +118,7 @@ struct Barriers {
   uint64_t pv_done[2];
   uint64_t mma_done;
   uint32_t tmem_base;
+  int4 ustash[8];       // per softmax warp: its unit's rows, first output row, first head
 };
 static_assert(sizeof(Barriers) <= 512, "barrier area");
 
@@ -257,7 +258,8 @@ template <int NH>
 __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const Params p) {
+                   const __grid_constant__ CUtensorMap tm_v,
+                   const __grid_constant__ CUtensorMap tm_o, const Params p) {
   using C = Cfg<NH>;
   constexpr int K = C::kThreads;
   extern __shared__ uint8_t smem_raw[];
@@ -351,6 +353,7 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
       prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);
+      prefetch_tensormap(&tm_o);
     }
     const int boxes = kBN / p.bs;                       // physical blocks per KV tile
     int gt = 0;                                         // KV tiles issued
@@ -518,11 +521,13 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
     const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
     int gt = 0;                                         // global key-tile index
     bool ok = true;
-    bool pending = false;                               // a row copy may still read `stage`
 
     for (int k = 0; ok; ++k) {
       Unit x;
       if (!next_unit(k, x)) break;
+      // the unit's place, for the output at its end (cheaper than deriving
+      // it again there, and no registers held through the tile loop)
+      if (lane == 0) B->ustash[warp] = make_int4(x.rows, x.q0 + x.row0, x.h0, 0);
       const int qpos = x.pos_first + r;
       const int pos_first = x.pos_first;
       const int ctx = x.ctx;
@@ -671,23 +676,29 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
       tmem_ld32(o_addr, o[0]);
       tmem_ld32(o_addr + 32, o[1]);
       tmem_ld_wait();
-      // the unit's rows and place, read again rather than held through the loop
-      unit_info<NH, K>(p, tab, static_cast<int>(unit_index(k, c, G)), x);
-      if (r < x.rows) {
-        float4* stage = reinterpret_cast<float4*>(smem + C::kStageOff + (hh * kBM + r) * kOPitch);
-        // the row goes out through its own staging row in shared memory with
-        // one 256-byte bulk copy (direct stores would scatter each warp
-        // instruction over 32 rows 8 KB apart)
-        if (pending) bulk_wait_read();                  // the previous copy has read it
-        const float inv = 1.0f / (l2.x + l2.y);
+      const int4 us = B->ustash[warp];                  // rows, first output row, first head
+      // Each warp stages its 32 rows in shared memory in the tensor-store
+      // layout (per head: two 64-column halves of 128 rows x 128 bytes, the
+      // 16-byte chunks of row r in 128-byte-swizzled order j ^ (r & 7), which
+      // is also free of bank conflicts), and its lane 0 hands them to the
+      // TMA engine as 16-row x 32-column tensor stores.  The softmax threads
+      // so spend only the staging on the unit's 64 KB of fp32 output.
+      const int r0 = wi * 32;                           // the warp's first row
+      const int nrows = min(32, us.x - r0);             // rows of it inside the unit
+      uint8_t* st_head = smem + C::kStageOff + hh * (kBM * kD * 4);
+      if (lane == 0) bulk_wait_read();                  // its last stores have read the rows
+      __syncwarp();
+      const float inv = 1.0f / (l2.x + l2.y);
+      if (lane < nrows) {
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc)
+        for (int half = 0; half < 2; ++half)
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            stage[cc * 8 + e / 4] =
-                make_float4(__uint_as_float(o[cc][e]) * inv, __uint_as_float(o[cc][e + 1]) * inv,
-                            __uint_as_float(o[cc][e + 2]) * inv,
-                            __uint_as_float(o[cc][e + 3]) * inv);
+          for (int jc = 0; jc < 8; ++jc)
+            *reinterpret_cast<float4*>(st_head + half * (kBM * 128) + r * 128 + ((jc ^ (r & 7)) << 4)) =
+                make_float4(__uint_as_float(o[half][4 * jc]) * inv,
+                            __uint_as_float(o[half][4 * jc + 1]) * inv,
+                            __uint_as_float(o[half][4 * jc + 2]) * inv,
+                            __uint_as_float(o[half][4 * jc + 3]) * inv);
         // A row that is not finite: a V value beyond the fp16 range of the
         // P.V product (bf16 holds values past 65504), or non-finite inputs.
         // The sum of the unnormalised row carries any inf or NaN.
@@ -701,14 +712,33 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
                                                        __uint_as_float(o[cc][e + 1])));
         const float2 c4 = __fadd2_rn(__fadd2_rn(chk[0], chk[1]), __fadd2_rn(chk[2], chk[3]));
         if (!isfinite(c4.x + c4.y) || !isfinite(inv)) report(p.status, TVL_DEV_NONFINITE);
-        fence_async_smem();
-        bulk_store(p.out + (static_cast<long long>(x.q0 + x.row0 + r) * p.hq + x.h0 + hh) * kD,
-                   stage, kD * 4);
+      }
+      fence_async_smem();                               // the staging, for the TMA engine
+      __syncwarp();
+      const int full = nrows >= 32 ? 32 : (nrows >= 16 ? 16 : 0);   // rows in whole 16-row groups
+      if (lane == 0 && full > 0) {
+        for (int g = 0; g < full; g += 16)
+#pragma unroll
+          for (int half = 0; half < 2; ++half)
+            tma_store_3d(&tm_o, st_head + half * (kBM * 128) + (r0 + g) * 128, half * 32, us.z + hh,
+                         us.y + r0 + g);
         bulk_commit();
-        pending = true;
+      }
+      if (lane >= full && lane < nrows) {
+        // a row outside the whole 16-row groups (a unit shorter than 128
+        // rows): straight from registers
+        float4* dst = reinterpret_cast<float4*>(
+            p.out + (static_cast<long long>(us.y + r) * p.hq + us.z + hh) * kD);
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            dst[cc * 8 + e / 4] =
+                make_float4(__uint_as_float(o[cc][e]) * inv, __uint_as_float(o[cc][e + 1]) * inv,
+                            __uint_as_float(o[cc][e + 2]) * inv, __uint_as_float(o[cc][e + 3]) * inv);
       }
     }
-    if (pending) bulk_wait_read();
+    if (lane == 0) bulk_wait_all();                     // the output stores are complete
     if (threadIdx.x == 0) {
       // units of sequences with inconsistent lengths were skipped: say so
       for (int k = 0;; ++k) {
@@ -745,11 +775,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
-              const cuuint64_t* strides, const cuuint32_t* box) {
+              const cuuint64_t* strides, const cuuint32_t* box,
+              CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+  CUresult r = fn(m, type, rank, const_cast<void*>(base), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -757,7 +788,8 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 
 template <int NH>
 cudaError_t launch_nh(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                      const Params& p, int num_seqs, int num_sms, cudaStream_t stream) {
+                      const CUtensorMap& to, const Params& p, int num_seqs, int num_sms,
+                      cudaStream_t stream) {
   using C = Cfg<NH>;
   // once per device: the shared-memory limit, and the check that the
   // register split fits the registers the block is launched with
@@ -785,14 +817,24 @@ cudaError_t launch_nh(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
   // behind a kernel that is still draining, they started over that kernel's
   // tail and the last to start set the end (chunked prefill after the paged
   // write: 176 us per step against 157 us).
-  prefill_kernel<NH><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+  prefill_kernel<NH><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
+  {
+    // the fp32 output [Tq, Hq, D]: 16-row x 32-column tiles of one head
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD),
+                                static_cast<cuuint64_t>(a.num_q_heads),
+                                static_cast<cuuint64_t>(a.total_q_tokens)};
+    const cuuint64_t strides[2] = {kD * 4, static_cast<cuuint64_t>(a.num_q_heads) * kD * 4};
+    const cuuint32_t box[3] = {32, 1, 16};
+    if (!make_map(&to, a.out, 3, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+      return cudaErrorInvalidValue;
+  }
   {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD),
                                 static_cast<cuuint64_t>(a.num_q_heads),
@@ -829,8 +871,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.n_qtiles = (a.max_q_len + kBM - 1) / kBM;
   p.scale_log2 = a.scale * kLog2e;
   p.status = a.status;
-  if (p.group >= 2) return launch_nh<2>(tq, tk, tv, p, a.num_seqs, a.num_sms, stream);
-  return launch_nh<1>(tq, tk, tv, p, a.num_seqs, a.num_sms, stream);
+  if (p.group >= 2) return launch_nh<2>(tq, tk, tv, to, p, a.num_seqs, a.num_sms, stream);
+  return launch_nh<1>(tq, tk, tv, to, p, a.num_seqs, a.num_sms, stream);
 }
 
 }  // namespace tvl
