@@ -26,8 +26,8 @@
 //             is then rescaled; exact, since one reference scales numerator
 //             and denominator).  P is stored as fp16 into TMEM once the
 //             previous P.V has consumed the buffer.  At a unit's end it
-//             normalises O and sends each row out of a staging row in
-//             shared memory with one bulk copy;
+//             normalises O into swizzled staging in shared memory, and each
+//             warp's 32 rows leave through four TMA tensor stores;
 //   4NH       producer: TMA loads of the Q tiles and, per 128-key tile, one
 //             box of bs tokens x 64 dims per physical block (K and V) found
 //             through the block table -- the paged gather; blocks past the
