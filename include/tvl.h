@@ -159,11 +159,14 @@ tvl_status tvl_paged_attention_decode_workspace_size(
  *   block_tables : int32 [S, MB]; context_lens : int32 [S] (device, read)
  * partition_size selects how the context is split (all splits are merged
  * exactly by log-sum-exp, the associative form of the online softmax):
- *   0   the library balances the total block count evenly over one CTA per
- *       SM; a sequence may be cut anywhere on a block boundary.
+ *   0   the library balances the blocks over one CTA per SM, each sequence
+ *       start counted as one 32-token stage more (its fixed cost); a
+ *       sequence may be cut anywhere on a block boundary.
  *   >0  fixed windows [p * P, (p + 1) * P) of P tokens from position 0 (the
  *       last one partial); P must be a multiple of block_size.  P >= MB * bs
- *       is a single pass per sequence and needs no workspace.
+ *       is a single pass per sequence and needs no workspace.  With more
+ *       windows than SMs, one CTA per SM walks them in equal contiguous
+ *       ranges; the results are the same either way.
  * workspace: device memory of at least the size reported by
  *   tvl_paged_attention_decode_workspace_size (may be NULL when that is 0);
  *   its contents on entry are ignored and on exit unspecified.
