@@ -528,6 +528,7 @@ __global__ void __launch_bounds__(Cfg<NH>::kThreads, 1)
       // the unit's place, for the output at its end (cheaper than deriving
       // it again there, and no registers held through the tile loop)
       if (lane == 0) B->ustash[warp] = make_int4(x.rows, x.q0 + x.row0, x.h0, 0);
+      __syncwarp();
       const int qpos = x.pos_first + r;
       const int pos_first = x.pos_first;
       const int ctx = x.ctx;
